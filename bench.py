@@ -1,0 +1,462 @@
+#!/usr/bin/env python
+"""Benchmark of the speculative-decoding verification step on GB300.
+
+One "step" is one full verification call (both phases: row statistics,
+then accept scan + final draw) over one synthetic batch already resident in
+HBM.  Default workload: c3 (B=64 sequences, k=5 drafts, V=151936, bf16
+logits, T=1), 213.9 MB of logits per step.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config c3]
+    python bench.py --impl reference ...    # the fp64 CPU oracle, host cores
+
+Prints one JSON line (rank 0).  value = logit GB/s (every logit read once),
+the metric the verification step is quoted in; steps/s, logits/s and the
+fraction of the measured HBM peak are reported beside it.
+
+Timing: W untimed warm-up steps, then K steps bracketed by a barrier and
+torch.cuda.synchronize() on both sides, CUDA events on the library's stream,
+max over ranks.  The inputs (214 MB) exceed the 126 MB L2 and two copies
+alternate between steps, so every step streams from HBM.  nvidia-smi clocks
+are sampled during the timed region.  With N > 1 (torchrun) every rank runs
+an independent replica on its own GPU (sequences are independent; there is
+no data-path collective) and value is the aggregate.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads  # noqa: E402
+
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "rows_kernel_c3.md")
+KERNEL_SOURCE = os.path.join(ROOT, "speculative_decoding_verification_top_gb300", "csrc",
+                             "spec_verify.cu")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", default="c3", choices=["c2", "c3", "c4", "c5"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="budget of the CPU-oracle baseline sample")
+    return ap.parse_args()
+
+
+def make_workload(name):
+    wl = workloads.CONFIGS[name]()
+    mode = "tree" if name == "c5" else "stochastic"
+    return wl, mode
+
+
+def describe(wl, mode):
+    if mode == "tree":
+        return {"workload": "%s: greedy tree verification, B=%d, N=%d nodes, V=%d, %s logits"
+                            % (wl.name, wl.B, wl.N, wl.V, wl.dtype),
+                "B": wl.B, "N": wl.N, "V": wl.V, "dtype": wl.dtype}
+    return {"workload": "%s: stochastic verification, B=%d, k=%d, V=%d, %s logits, T=%g, top_p=%g"
+                        % (wl.name, wl.B, wl.k, wl.V, wl.dtype, wl.T, wl.top_p),
+            "B": wl.B, "k": wl.k, "V": wl.V, "dtype": wl.dtype, "T": wl.T, "top_p": wl.top_p}
+
+
+# ------------------------------------------------------------ distributed
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 20 ms."""
+    FIELDS = ("index,timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.path = tempfile.mktemp(suffix=".csv")
+        self.proc = None
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "20"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        self.proc.wait()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[2]), smax=float(parts[3]), power=float(parts[4]),
+                                 hw=parts[6], hwt=parts[7], swt=parts[8], cap=parts[9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("cap", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median([r["sm"] for r in rows])),
+                "sm_max_mhz": max(r["smax"] for r in rows),
+                "power_w_max": max(r["power"] for r in rows),
+                "samples": len(rows), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------- peaks
+
+def hbm_peak():
+    try:
+        with open(PEAKS_FILE) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def profiled_traffic():
+    """dram bytes per rows_kernel launch from the committed ncu summary, if it
+    was taken on the current kernel source (else None)."""
+    try:
+        text = open(PROFILE_SUMMARY).read()
+        src = hashlib.sha256(open(KERNEL_SOURCE, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    fields = {}
+    for line in text.splitlines():
+        if line.startswith("traffic_bytes_per_launch:") or line.startswith("source_sha256_16:"):
+            k, v = line.split(":", 1)
+            fields[k.strip()] = v.strip()
+    if fields.get("source_sha256_16") != src or "traffic_bytes_per_launch" not in fields:
+        return None
+    return float(fields["traffic_bytes_per_launch"])
+
+
+# ---------------------------------------------------------------- our arm
+
+def to_dev(a, dev):
+    import torch
+    if a.dtype == np.uint16:
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+    return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+
+class Job:
+    """Device buffers and bound launchers for one workload."""
+
+    def __init__(self, wl, mode, dev):
+        import torch
+        import speculative_decoding_verification_top_gb300 as sv
+        self.sv, self.wl, self.mode, self.dev = sv, wl, mode, dev
+        self.stream = torch.cuda.current_stream(dev)
+        self.sets = []
+        if mode == "tree":
+            base = (to_dev(wl.target, dev), to_dev(wl.parents, dev), to_dev(wl.node_tokens, dev))
+            self.sets = [base, (base[0].clone(), base[1], base[2])]
+            W = wl.D + 1
+            self.out_t = torch.empty((wl.B, W), dtype=torch.int32, device=dev)
+            self.out_n = torch.empty((wl.B,), dtype=torch.int32, device=dev)
+            self.out_p = torch.empty((wl.B, W), dtype=torch.int32, device=dev)
+            nbytes = sv.spec_verify_tree_workspace_size(wl.B, wl.N, wl.V)
+            self.launches_per_step = 2
+        else:
+            base = (to_dev(wl.target, dev), to_dev(wl.draft, dev), to_dev(wl.draft_tokens, dev),
+                    to_dev(wl.uniforms, dev))
+            self.sets = [base, (base[0].clone(), base[1].clone(), base[2], base[3])]
+            self.out_t = torch.empty((wl.B, wl.k + 1), dtype=torch.int32, device=dev)
+            self.out_n = torch.empty((wl.B,), dtype=torch.int32, device=dev)
+            nbytes = sv.spec_verify_workspace_size(wl.B, wl.k, wl.V)
+            self.launches_per_step = 2
+        self.ws = sv.new_workspace(nbytes, dev)
+        self.dtype = sv.SPEC_BF16 if wl.dtype == workloads.BF16 else sv.SPEC_F32
+
+    def chain_args(self, i):
+        t, d, x, u = self.sets[i % 2]
+        wl, sv = self.wl, self.sv
+        return (t.data_ptr(), d.data_ptr(), x.data_ptr(), u.data_ptr(), wl.B, wl.k, wl.V, wl.T,
+                wl.top_p, sv.SPEC_STOCHASTIC, self.dtype, self.out_t.data_ptr(),
+                self.out_n.data_ptr(), self.ws.data_ptr(), self.ws.numel(),
+                self.stream.cuda_stream)
+
+    def step(self, i):
+        sv = self.sv
+        if self.mode == "tree":
+            t, p, x = self.sets[i % 2]
+            wl = self.wl
+            sv.spec_verify_tree(t.data_ptr(), p.data_ptr(), x.data_ptr(), wl.B, wl.N, wl.V, wl.D,
+                                self.dtype, self.out_t.data_ptr(), self.out_n.data_ptr(),
+                                self.out_p.data_ptr(), self.ws.data_ptr(), self.ws.numel(),
+                                self.stream.cuda_stream)
+        else:
+            sv.spec_verify_sample(*self.chain_args(i))
+
+    def phases(self, i, ev_mid_a, ev_mid_b):
+        """One chain step as its two phases, events around the row kernel."""
+        args = self.chain_args(i)
+        ev_mid_a.record(self.stream)
+        self.sv.spec_verify_sample_rows(*args)
+        ev_mid_b.record(self.stream)
+        self.sv.spec_verify_sample_finish(*args)
+
+
+def timed_device(job, steps, warmup, world):
+    import torch
+    for i in range(warmup):
+        job.step(i)
+    torch.cuda.synchronize()
+    chain = job.mode != "tree"
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    mids = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(steps)] if chain else []
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0.record(job.stream)
+    for i in range(steps):
+        if chain:
+            job.phases(i, *mids[i])
+        else:
+            job.step(i)
+    ev1.record(job.stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    total_ms = ev0.elapsed_time(ev1)
+    rows_ms = float(np.mean([a.elapsed_time(b) for a, b in mids])) if chain else None
+    return total_ms, rows_ms
+
+
+def timed_e2e(job, steps):
+    """Host buffers -> device -> library call -> results back to the host."""
+    import torch
+    wl = job.wl
+    def pinned(a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:  # bf16 bit patterns
+            a = a.view(np.int16)
+        return torch.from_numpy(a).pin_memory()
+
+    if job.mode == "tree":
+        host_in = [pinned(a) for a in (wl.target, wl.parents, wl.node_tokens)]
+        outs = (job.out_t, job.out_n, job.out_p)
+    else:
+        host_in = [pinned(a) for a in (wl.target, wl.draft, wl.draft_tokens, wl.uniforms)]
+        outs = (job.out_t, job.out_n)
+    dev_in = job.sets[0]
+    host_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+    views = [d.view(torch.int16) if d.dtype == torch.bfloat16 else d for d in dev_in]
+    h2d = sum(h.numel() * h.element_size() for h in host_in)
+    d2h = sum(h.numel() * h.element_size() for h in host_out)
+
+    def one():
+        for h, d in zip(host_in, views):
+            d.copy_(h, non_blocking=True)
+        job.step(0)
+        for h, o in zip(host_out, outs):
+            h.copy_(o, non_blocking=True)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    e0.record(job.stream)
+    for _ in range(steps):
+        one()
+    e1.record(job.stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    return e0.elapsed_time(e1), wall * 1e3, h2d, d2h
+
+
+def cpu_baseline(wl, mode, seconds):
+    """The fp64 oracle, as it stands, on one host core over a bounded sample:
+    whole sequences of the same workload, round-robin, until `seconds`."""
+    import oracle
+    oracle.build()
+    done, bytes_done, t0 = 0, 0, time.perf_counter()
+    while True:
+        b = done % wl.B
+        sl = slice(b, b + 1)
+        if mode == "tree":
+            oracle.verify_tree(wl.target[sl], wl.parents, wl.node_tokens[sl], wl.D)
+            bytes_done += wl.N * wl.V * (4 if wl.dtype == workloads.F32 else 2)
+        else:
+            oracle.verify_sample(wl.target[sl], wl.draft[sl], wl.draft_tokens[sl],
+                                 wl.uniforms[sl], T=wl.T, top_p=wl.top_p)
+            bytes_done += wl.logit_bytes() // wl.B
+        done += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return {"value": bytes_done / el / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": "%d whole sequences of %s (round-robin over the batch), %.1f s on one core"
+                      % (done, wl.name, el),
+            "host_cores": os.cpu_count()}
+
+
+def run_ours(args):
+    import torch
+    import speculative_decoding_verification_top_gb300 as sv
+    world, rank, local = dist_setup()
+    sv.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wl, mode = make_workload(args.config)
+    job = Job(wl, mode, dev)
+    job.step(0)
+    torch.cuda.synchronize()
+
+    visible = os.environ.get("CUDA_VISIBLE_DEVICES")
+    smi_index = visible.split(",")[local] if visible else str(local)
+    clocks = ClockSampler(smi_index)
+    time.sleep(0.3)
+    total_ms, rows_ms = timed_device(job, args.steps, args.warmup, world)
+    clk = clocks.stop()
+    total_ms = max_over_ranks(total_ms, world)
+
+    nbytes = wl.logit_bytes(mode)
+    ms_step = total_ms / args.steps
+    value = world * nbytes * args.steps / (total_ms * 1e-3) / 1e9
+    peak, peak_kind = hbm_peak()
+    e2e_ms, e2e_wall_ms, h2d, d2h = timed_e2e(job, args.e2e_steps)
+    e2e_ms = max_over_ranks(e2e_ms, world)
+    e2e_value = world * nbytes * args.e2e_steps / (e2e_ms * 1e-3) / 1e9
+
+    if rows_ms is not None:
+        achieved = nbytes / (rows_ms * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "kernel": "rows_kernel", "achieved": round(achieved, 1),
+                    "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                    "frac": round(achieved / peak, 4), "traffic": profiled_traffic(),
+                    "algorithmic_bytes": nbytes, "avg_launch_us": round(rows_ms * 1e3, 2)}
+    else:
+        per_launch_ms = ms_step  # the tree call: argmax rows kernel dominates
+        achieved = nbytes / (per_launch_ms * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "kernel": "rows_kernel+tree_kernel", "achieved": round(achieved, 1),
+                    "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                    "frac": round(achieved / peak, 4), "traffic": None,
+                    "algorithmic_bytes": nbytes, "avg_launch_us": round(per_launch_ms * 1e3, 2)}
+
+    out = {
+        "metric": "verify logits GB/s (% of GB300 HBM peak) and verify steps/sec at (B,k,V)",
+        "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+        "impl": "ours",
+        "config": dict(describe(wl, mode), l2="inputs %d MB > 126 MB L2, two input copies "
+                       "alternate between steps" % (nbytes // 10**6)),
+        "frac_of_peak": round(value / world / peak, 4), "peak_gbs": peak, "peak_kind": peak_kind,
+        "frac_of_nominal_8tbs": round(value / world / 8000.0, 4),
+        "verify_calls_per_s": round(world * args.steps / (total_ms * 1e-3), 1),
+        "sequence_steps_per_s": round(world * wl.B * args.steps / (total_ms * 1e-3), 1),
+        "logits_per_s": round(value * 1e9 / (2 if wl.dtype == workloads.BF16 else 4), 1),
+        "roofline": roofline,
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "steps": args.e2e_steps,
+                "ms_per_step": round(e2e_ms / args.e2e_steps, 4),
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": job.launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1:
+        out["cpu_baseline"] = cpu_baseline(wl, mode, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+def run_reference(args):
+    world, rank, _ = (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")), 0)
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    wl, mode = make_workload(args.config)
+    per_seq = wl.logit_bytes(mode) // wl.B
+
+    def one(i):
+        sl = slice(i % wl.B, i % wl.B + 1)
+        if mode == "tree":
+            oracle.verify_tree(wl.target[sl], wl.parents, wl.node_tokens[sl], wl.D)
+        else:
+            oracle.verify_sample(wl.target[sl], wl.draft[sl], wl.draft_tokens[sl],
+                                 wl.uniforms[sl], T=wl.T, top_p=wl.top_p)
+
+    for i in range(args.warmup):
+        one(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        one(i)
+    el = time.perf_counter() - t0
+    value = per_seq * args.steps / el / 1e9
+    sample = ("each step: one whole sequence of %s (round-robin over the batch) through the "
+              "fp64 CPU oracle, one core" % wl.name)
+    out = {
+        "metric": "verify logits GB/s (% of GB300 HBM peak) and verify steps/sec at (B,k,V)",
+        "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(el * 1e3 / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "impl": "reference", "config": describe(wl, mode),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    a = parse()
+    if a.impl == "reference":
+        run_reference(a)
+    else:
+        run_ours(a)

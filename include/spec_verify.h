@@ -1,0 +1,235 @@
+/*
+ * spec_verify.h -- C ABI of the GB300 (sm_103a) speculative-decoding
+ * verification library, libspecverify.so.
+ *
+ * The library implements the target-side verification step of speculative
+ * decoding as described on these pages (cited by title and section):
+ *   [LZ] "3.5 Speculative Decoding" (llm-learning-path)
+ *   [MN] "246 Speculative Decoding" (ai_in_action)
+ *   [LB] "Speculative Decoding: Mathematical Foundations, Rejection Sampling
+ *        Dynamics, Draft Architectures, and Serving Latency" (llms.blog)
+ *   [SS] "Speculative Decoding from First Principles" (theservingstack.com)
+ *
+ * Conventions shared by every entry point
+ *   - All array arguments are DEVICE pointers into memory the caller owns
+ *     (e.g. PyTorch tensors).  The library never allocates, frees or
+ *     synchronises, except spec_verify_last_error, which synchronises the
+ *     given stream.  Work is enqueued on `stream` (NULL = the legacy default
+ *     stream) and completes asynchronously.
+ *   - Logit arrays are row-major with the vocabulary innermost and
+ *     contiguous; their base pointers must be aligned to their element size
+ *     (4 bytes for SPEC_F32, 2 for SPEC_BF16 -- bf16 is stored as its 16-bit
+ *     pattern).  Token arrays are int32, uniforms fp32.
+ *   - Argument errors are returned synchronously as a negative status and
+ *     nothing is enqueued.  Data errors found on the device (a NaN or +inf
+ *     logit, a row that is entirely -inf, a token outside [0, V), a uniform
+ *     outside [0, 1), a malformed tree) never trap: the affected sequence's
+ *     outputs are set to -1 and a bit is OR-ed into the workspace's error
+ *     word, read back by spec_verify_last_error.
+ *   - A workspace is caller-owned device memory of at least the size the
+ *     matching *_workspace_size function reports.  It must be zero-filled
+ *     before its first use (spec_verify_workspace_init, or any zero fill);
+ *     the library returns its internal counters to zero at the end of every
+ *     call.  Calls that share one workspace must be ordered (one stream, or
+ *     events): two calls running at the same time on one workspace race.
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (the same type as cudaStream_t). */
+typedef struct CUstream_st *spec_stream_t;
+
+/* Logit storage types. */
+enum { SPEC_F32 = 0, SPEC_BF16 = 1 };
+
+/* Verification rules for spec_verify_sample. */
+enum {
+    SPEC_STOCHASTIC = 0, /* rejection sampling with residual / bonus draw */
+    SPEC_GREEDY = 1      /* draft kept iff it equals the target argmax     */
+};
+
+/* Synchronous status codes (negative: nothing was enqueued). */
+enum {
+    SPEC_OK = 0,
+    SPEC_ERR_NULL = -1,      /* a required pointer is NULL                 */
+    SPEC_ERR_SHAPE = -2,     /* B, k, V, N or D outside the supported range */
+    SPEC_ERR_PARAM = -3,     /* temperature <= 0 or not finite, top_p not
+                                in (0, 1]                                  */
+    SPEC_ERR_DTYPE = -4,     /* dtype not SPEC_F32 / SPEC_BF16             */
+    SPEC_ERR_MODE = -5,      /* mode not SPEC_STOCHASTIC / SPEC_GREEDY     */
+    SPEC_ERR_ALIGN = -6,     /* a pointer misaligned for its element type  */
+    SPEC_ERR_WORKSPACE = -7, /* workspace NULL or smaller than required    */
+    SPEC_ERR_CUDA = -8       /* a CUDA runtime call failed                 */
+};
+
+/* Data-error bits of the workspace error word (device-detected). */
+enum {
+    SPEC_DATA_ROW_NONFINITE = 1 << 1,   /* a NaN or +inf logit in a row    */
+    SPEC_DATA_ROW_ALL_NEG_INF = 1 << 2, /* every logit of a row is -inf    */
+    SPEC_DATA_TOKEN_RANGE = 1 << 3,     /* a draft or node token not in
+                                           [0, V)                          */
+    SPEC_DATA_UNIFORM_RANGE = 1 << 4,   /* a uniform not in [0, 1)         */
+    SPEC_DATA_TREE_SHAPE = 1 << 5       /* parents not a rooted tree in
+                                           topological order, or a node
+                                           deeper than D                   */
+};
+
+/* Supported ranges. */
+#define SPEC_MAX_K 31          /* draft length k in [1, 31]: the k+1
+                                  positions fit one warp                  */
+#define SPEC_MAX_V (1 << 22)   /* vocabulary size V in [1, 2^22]           */
+#define SPEC_MAX_TREE_NODES 1024
+
+/*
+ * Workspace bytes needed by spec_verify_sample for batch B, draft length k
+ * and vocabulary V (either mode, either dtype).  Returns SPEC_OK or
+ * SPEC_ERR_NULL / SPEC_ERR_SHAPE.
+ */
+int spec_verify_workspace_size(int B, int k, int V, size_t *bytes);
+
+/* Workspace bytes needed by spec_verify_tree for B trees of N nodes. */
+int spec_verify_tree_workspace_size(int B, int N, int V, size_t *bytes);
+
+/* Zero-fill `bytes` of a workspace on `stream` (cudaMemsetAsync). */
+int spec_verify_workspace_init(void *workspace, size_t bytes, spec_stream_t stream);
+
+/*
+ * One verification step for B independent sequences.
+ *
+ * SPEC_STOCHASTIC -- [LZ] "The algorithm (one step)", steps 3 and 4; [MN]
+ * 2.2 "The acceptance test for one token" and 3.3 "The full block loop";
+ * [LB] "The Modified Rejection Sampling Algorithm":
+ *   p_i = the target distribution at position i (row i of target_logits),
+ *   q_i = the draft distribution (row i of draft_logits), both after the
+ *   same processing ([LZ] "Notation"; [MN] 6 "Pitfalls"): divide the logits
+ *   by `temperature`, softmax, then -- if top_p < 1 -- keep the smallest set
+ *   of most likely tokens whose mass reaches top_p (all tokens tied with the
+ *   last one kept) and renormalise.
+ *   For i = 1..k, left to right: accept draft x~_i iff
+ *     u_i * q_i(x~_i) < p_i(x~_i)        (u_i = uniforms[b][i-1])
+ *   and stop at the first rejection.  j = number accepted.
+ *   If j < k: draw from the residual max(0, p_{j+1} - q_{j+1}) normalised
+ *   (if it is zero everywhere, from p_{j+1}); if j = k: draw the bonus
+ *   token from p_{k+1}.  The draw uses u = uniforms[b][k] by inverse CDF in
+ *   token order: the smallest x whose cumulative weight exceeds u * (total
+ *   weight).
+ * SPEC_GREEDY -- [LZ] end of "Proof that the output distribution is exactly
+ * p"; [SS] "Draft, verify, keep what matches": g_i = first argmax of the raw
+ * target row i; j = number of leading i with x~_i == g_i; the emitted token
+ * after them is g_{j+1}.  draft_logits, uniforms, temperature and top_p are
+ * ignored (may be NULL / any value).
+ *
+ * Arguments
+ *   target_logits    [B, k+1, V] dtype, device
+ *   draft_logits     [B, k, V]   dtype, device (STOCHASTIC)
+ *   draft_tokens     [B, k]      int32, device
+ *   uniforms         [B, k+1]    fp32 in [0, 1), device (STOCHASTIC)
+ *   B >= 0, 1 <= k <= SPEC_MAX_K, 1 <= V <= SPEC_MAX_V
+ *   temperature > 0, 0 < top_p <= 1 (STOCHASTIC)
+ *   mode             SPEC_STOCHASTIC or SPEC_GREEDY
+ *   dtype            SPEC_F32 or SPEC_BF16 (both logit arrays)
+ *   out_tokens       [B, k+1] int32, device: x~_1..x~_j, then the drawn
+ *                    (or argmax) token, then -1; all -1 on a data error
+ *   out_num_accepted [B] int32, device: j in [0, k], -1 on a data error
+ *   workspace        >= spec_verify_workspace_size(B, k, V) bytes, zeroed
+ *                    before first use
+ * Returns SPEC_OK or a negative status.
+ */
+int spec_verify_sample(const void *target_logits, const void *draft_logits,
+                       const int32_t *draft_tokens, const float *uniforms,
+                       int B, int k, int V, float temperature, float top_p,
+                       int mode, int dtype, int32_t *out_tokens,
+                       int32_t *out_num_accepted, void *workspace,
+                       size_t workspace_bytes, spec_stream_t stream);
+
+/*
+ * The two phases of spec_verify_sample, with the same arguments.
+ * spec_verify_sample == spec_verify_sample_rows followed, on the same
+ * stream and workspace, by spec_verify_sample_finish.
+ *   _rows    streams every logit row once and leaves per-row statistics
+ *            (max, normaliser, nucleus threshold, argmax) in the workspace;
+ *   _finish  reads them, runs the accept scan and the final draw, and
+ *            writes out_tokens / out_num_accepted.
+ * The split lets a caller time or overlap the phases; _finish must follow a
+ * _rows call with identical arguments, with no other call on the workspace
+ * in between.
+ */
+int spec_verify_sample_rows(const void *target_logits, const void *draft_logits,
+                            const int32_t *draft_tokens, const float *uniforms,
+                            int B, int k, int V, float temperature, float top_p,
+                            int mode, int dtype, int32_t *out_tokens,
+                            int32_t *out_num_accepted, void *workspace,
+                            size_t workspace_bytes, spec_stream_t stream);
+int spec_verify_sample_finish(const void *target_logits, const void *draft_logits,
+                              const int32_t *draft_tokens, const float *uniforms,
+                              int B, int k, int V, float temperature, float top_p,
+                              int mode, int dtype, int32_t *out_tokens,
+                              int32_t *out_num_accepted, void *workspace,
+                              size_t workspace_bytes, spec_stream_t stream);
+
+/*
+ * Greedy tree verification for B sequences sharing one candidate tree --
+ * [LZ] "Tree verification": the flattened tree is scored in one target
+ * pass; keep the longest root-to-leaf path that passes verification; [LB]
+ * "Tree-Based Verification and Custom Attention Masks".
+ *   g_n = first argmax of target row n.  Node c (parent n) is accepted iff
+ *   n is accepted and node_tokens[b][c] == g_n; the root is accepted.  The
+ *   deepest accepted node wins (ties to the lowest flattened index); its
+ *   path's tokens are emitted, then g of that node (the bonus token).
+ *
+ * Arguments
+ *   target_logits    [B, N, V] dtype, device: one row per flattened node
+ *   parents          [N] int32, device: parents[0] = -1 (the root, the last
+ *                    committed token), 0 <= parents[n] < n otherwise
+ *   node_tokens      [B, N] int32, device: candidate token of each node (the
+ *                    root's entry is ignored)
+ *   1 <= N <= SPEC_MAX_TREE_NODES, 0 <= D < N: every node's depth <= D
+ *   out_tokens       [B, D+1] int32, device: path tokens, bonus, -1 pad
+ *   out_num_accepted [B] int32, device: accepted depth d, -1 on a data error
+ *   out_path         [B, D+1] int32, device, or NULL: node ids root, n_1,
+ *                    ..., n_d, then -1
+ *   workspace        >= spec_verify_tree_workspace_size(B, N, V) bytes
+ * Returns SPEC_OK or a negative status.
+ */
+int spec_verify_tree(const void *target_logits, const int32_t *parents,
+                     const int32_t *node_tokens, int B, int N, int V, int D,
+                     int dtype, int32_t *out_tokens, int32_t *out_num_accepted,
+                     int32_t *out_path, void *workspace, size_t workspace_bytes,
+                     spec_stream_t stream);
+
+/*
+ * Synchronise `stream`, then return the workspace's data-error word (an OR
+ * of SPEC_DATA_* bits accumulated since the previous call of this function;
+ * 0 if none) and clear it.  Negative on an argument or CUDA error.
+ */
+int spec_verify_last_error(void *workspace, size_t workspace_bytes, spec_stream_t stream);
+
+/*
+ * Debug read-out of the intermediates of the last spec_verify_sample call
+ * (STOCHASTIC) made with this workspace and the same B, k, V:
+ *   P [B, k]    p_i(x~_i), processed target probability of each draft
+ *   Q [B, k]    q_i(x~_i)
+ *   Z [B, 2k+1] per-row normaliser sum_x exp((l(x) - max l) / T) over the
+ *               kept tokens (target rows 0..k, then draft rows 0..k-1)
+ *   S [B]       total weight of the final draw (residual or bonus row)
+ * All four are device fp32 arrays (any may be NULL).  Enqueued on `stream`.
+ */
+int spec_verify_intermediates(const void *workspace, size_t workspace_bytes,
+                              int B, int k, int V, float *P, float *Q, float *Z,
+                              float *S, spec_stream_t stream);
+
+/* Static, human-readable description of a status or data-error bit. */
+const char *spec_verify_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

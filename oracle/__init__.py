@@ -181,3 +181,32 @@ def verify_tree(target, parents, node_tokens, depth):
     if err < 0:
         raise ValueError("oracle_verify_tree rejected its arguments")
     return dict(tokens=out_t, num_accepted=out_n, path=out_p, errors=err)
+
+
+def boundary_flags(res, uniforms, top_p=1.0, tol=1e-5):
+    """Sequences whose outcome sits within `tol` of a decision boundary.
+
+    A float32 implementation may legitimately decide such a sequence
+    differently from this fp64 oracle.  Flagged when, at any accept test the
+    oracle ran, |u_i - P_i / Q_i| < tol; or when |u - C(x-1)/S| or
+    |u - C(x)/S| < tol at the drawn token x; or (top-p) when a row's
+    cumulative mass before or at the threshold is within tol of top_p.
+    `res` must come from verify_sample(..., debug=True).
+    """
+    dbg, info = res["dbg"], res["row_info"]
+    B = dbg.shape[0]
+    k = (dbg.shape[1] - 3) // 2
+    u = np.asarray(uniforms, np.float64).reshape(B, k + 1)
+    j = res["num_accepted"]
+    P, Q = dbg[:, :k], dbg[:, k:2 * k]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        ratio = np.where(Q > 0, P / Q, np.inf)
+    tested = np.arange(k)[None, :] <= np.minimum(j, k - 1)[:, None]
+    flag = np.any(tested & (np.abs(u[:, :k] - ratio) < tol), axis=1)
+    S, c0, c1 = dbg[:, 2 * k], dbg[:, 2 * k + 1], dbg[:, 2 * k + 2]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        flag |= (np.abs(u[:, k] - c0 / S) < tol) | (np.abs(u[:, k] - c1 / S) < tol)
+    if top_p < 1.0:
+        near = (np.abs(info[:, :, 2] - top_p) < tol) | (np.abs(info[:, :, 3] - top_p) < tol)
+        flag |= np.any(near, axis=1)
+    return flag & (j >= 0)
