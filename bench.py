@@ -43,8 +43,8 @@ PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 7900.0
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "rows_kernel_c3.md")
-KERNEL_SOURCE = os.path.join(ROOT, "speculative_decoding_verification_top_gb300", "csrc",
-                             "spec_verify.cu")
+KERNEL_SOURCES = [os.path.join(ROOT, "speculative_decoding_verification_top_gb300", "csrc", f)
+                  for f in ("common.cuh", "rows.cu")]
 
 
 def parse():
@@ -170,7 +170,10 @@ def profiled_traffic():
     was taken on the current kernel source (else None)."""
     try:
         text = open(PROFILE_SUMMARY).read()
-        src = hashlib.sha256(open(KERNEL_SOURCE, "rb").read()).hexdigest()[:16]
+        h = hashlib.sha256()
+        for path in KERNEL_SOURCES:
+            h.update(open(path, "rb").read())
+        src = h.hexdigest()[:16]
     except OSError:
         return None
     fields = {}

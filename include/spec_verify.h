@@ -21,7 +21,8 @@
  *     (4 bytes for SPEC_F32, 2 for SPEC_BF16 -- bf16 is stored as its 16-bit
  *     pattern).  Token arrays are int32, uniforms fp32.
  *   - Argument errors are returned synchronously as a negative status and
- *     nothing is enqueued.  Data errors found on the device (a NaN or +inf
+ *     nothing is enqueued.  A call with B = 0 is valid, enqueues nothing and
+ *     may pass NULL for every array.  Data errors found on the device (a NaN or +inf
  *     logit, a row that is entirely -inf, a token outside [0, V), a uniform
  *     outside [0, 1), a malformed tree) never trap: the affected sequence's
  *     outputs are set to -1 and a bit is OR-ed into the workspace's error
@@ -159,7 +160,8 @@ int spec_verify_sample(const void *target_logits, const void *draft_logits,
  *            writes out_tokens / out_num_accepted.
  * The split lets a caller time or overlap the phases; _finish must follow a
  * _rows call with identical arguments, with no other call on the workspace
- * in between.
+ * in between.  In SPEC_GREEDY mode _rows does all the work and _finish
+ * enqueues nothing.
  */
 int spec_verify_sample_rows(const void *target_logits, const void *draft_logits,
                             const int32_t *draft_tokens, const float *uniforms,

@@ -24,9 +24,12 @@ import subprocess
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _ROOT = os.path.dirname(_PKG)
 LIB_PATH = os.path.join(_PKG, "libspecverify.so")
-SOURCES = [os.path.join(_PKG, "csrc", "spec_verify.cu")]
+CSRC = os.path.join(_PKG, "csrc")
+SOURCES = [os.path.join(CSRC, f) for f in ("api.cu", "rows.cu", "final.cu")]
+HEADERS = [os.path.join(CSRC, "common.cuh")]
 INCLUDE = os.path.join(_ROOT, "include")
 HEADER = os.path.join(INCLUDE, "spec_verify.h")
+BUILD_DIR = os.path.join(_PKG, "_build")
 
 SPEC_F32, SPEC_BF16 = 0, 1
 SPEC_STOCHASTIC, SPEC_GREEDY = 0, 1
@@ -51,10 +54,9 @@ EXPORTED = (
     "spec_verify_status_string",
 )
 
-NVCC_FLAGS = [
-    "-O3", "-std=c++17", "-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo",
-    "-Xcompiler", "-fPIC", "-shared",
-]
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+NVCC_FLAGS = ["-O3", "-std=c++17", *ARCH, "-lineinfo", "-Xcompiler", "-fPIC",
+              "-Xcompiler", "-fvisibility=hidden"]
 
 
 class SpecVerifyError(RuntimeError):
@@ -62,16 +64,28 @@ class SpecVerifyError(RuntimeError):
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile the CUDA sources into libspecverify.so (in-tree) with nvcc."""
-    newest = max(os.path.getmtime(p) for p in SOURCES + [HEADER])
+    """Compile the CUDA sources for sm_103a (one nvcc per translation unit,
+    in parallel) and link libspecverify.so in-tree."""
+    newest = max(os.path.getmtime(p) for p in SOURCES + HEADERS + [HEADER])
     if not force and os.path.exists(LIB_PATH) and os.path.getmtime(LIB_PATH) >= newest:
         return LIB_PATH
-    tmp = LIB_PATH + ".%d.tmp" % os.getpid()
-    cmd = ["nvcc", *NVCC_FLAGS, "-I", INCLUDE, *SOURCES, "-o", tmp]
-    if verbose:
-        cmd.insert(1, "-Xptxas=-v")
-    subprocess.check_call(cmd)
+    os.makedirs(BUILD_DIR, exist_ok=True)
+    tag = "%d" % os.getpid()
+    objs, procs = [], []
+    for src in SOURCES:
+        obj = os.path.join(BUILD_DIR, os.path.basename(src) + "." + tag + ".o")
+        cmd = ["nvcc", *NVCC_FLAGS, "-I", INCLUDE, "-c", src, "-o", obj]
+        if verbose:
+            cmd.insert(1, "-Xptxas=-v")
+        objs.append(obj)
+        procs.append(subprocess.Popen(cmd))
+    if any(p.wait() != 0 for p in procs):
+        raise RuntimeError("nvcc failed")
+    tmp = LIB_PATH + "." + tag + ".tmp"
+    subprocess.check_call(["nvcc", *ARCH, "-shared", *objs, "-o", tmp])
     os.replace(tmp, LIB_PATH)
+    for obj in objs:
+        os.unlink(obj)
     return LIB_PATH
 
 

@@ -1,0 +1,324 @@
+// api.cu -- the C ABI of libspecverify.so (declared in include/spec_verify.h):
+// argument validation, workspace layout and kernel dispatch.  No compute.
+
+#include "common.cuh"
+
+#define SPEC_EXPORT extern "C" __attribute__((visibility("default")))
+
+namespace specv {
+namespace {
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+int tiles_for(int V) { return (V + kTileMax - 1) / kTileMax; }
+int tile_len(int V, int T) { return ((V + T - 1) / T + 7) / 8 * 8; }
+int subs_for(int V) { return (V + kSubW - 1) / kSubW; }
+// Partial slots per row: a row of V elements meets at most ceil(V / seg) + 1
+// warp segments (seg >= kMinSeg), and at most tiles_for(V) CTA tiles.
+int pmax_for(int V) { return (V + kMinSeg - 1) / kMinSeg + 2; }
+
+// Carve the workspace; returns the bytes needed (base may be null).
+size_t carve(void *base, int B, int rows_per_seq, int V, Workspace *ws) {
+    const size_t rows = static_cast<size_t>(B) * rows_per_seq;
+    const int pmax = pmax_for(V), NS = subs_for(V);
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off = align_up(off + bytes);
+        return static_cast<char *>(base) + o;
+    };
+    char *err = take(kAlign);
+    char *row_ctr = take(rows * sizeof(uint32_t));
+    char *seq_rows = take(static_cast<size_t>(B) * sizeof(uint32_t));
+    char *seq_ctr = take(static_cast<size_t>(B) * sizeof(uint32_t));
+    char *partial = take(rows * pmax * sizeof(Partial));
+    char *rowrec = take(rows * sizeof(RowRec));
+    char *subs = take(static_cast<size_t>(B) * NS * sizeof(float));
+    char *seqs = take(static_cast<size_t>(B) * sizeof(SeqRec));
+    if (ws) {
+        ws->err = reinterpret_cast<uint32_t *>(err);
+        ws->row_ctr = reinterpret_cast<uint32_t *>(row_ctr);
+        ws->seq_rows = reinterpret_cast<uint32_t *>(seq_rows);
+        ws->seq_ctr = reinterpret_cast<uint32_t *>(seq_ctr);
+        ws->partial = reinterpret_cast<Partial *>(partial);
+        ws->rows = reinterpret_cast<RowRec *>(rowrec);
+        ws->sub_sums = reinterpret_cast<float *>(subs);
+        ws->seqs = reinterpret_cast<SeqRec *>(seqs);
+        ws->pmax = pmax;
+    }
+    return off;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool chain_sizes_ok(int B, int k, int V) {
+    if (B < 0 || k < 1 || k > SPEC_MAX_K || V < 1 || V > SPEC_MAX_V) return false;
+    const long long rows = static_cast<long long>(B) * (2 * k + 1);
+    return rows * tiles_for(V) < INT_MAX && static_cast<long long>(B) * subs_for(V) * 32 < INT_MAX;
+}
+
+bool tree_sizes_ok(int B, int N, int V) {
+    if (B < 0 || N < 1 || N > SPEC_MAX_TREE_NODES || V < 1 || V > SPEC_MAX_V) return false;
+    return static_cast<long long>(B) * N * tiles_for(V) < INT_MAX;
+}
+
+struct ChainPlan {
+    RowView rows;
+    SeqArgs seq;
+    Workspace ws;
+    FinalArgs fin;
+    int stoch, dtype, rows_total, use_topp;
+    float c, temperature, top_p;
+    cudaStream_t st;
+};
+
+int plan_chain(const void *target_logits, const void *draft_logits, const int32_t *draft_tokens,
+               const float *uniforms, int B, int k, int V, float temperature, float top_p,
+               int mode, int dtype, int32_t *out_tokens, int32_t *out_num_accepted,
+               void *workspace, size_t workspace_bytes, spec_stream_t stream, ChainPlan *plan) {
+    if (mode != SPEC_STOCHASTIC && mode != SPEC_GREEDY) return SPEC_ERR_MODE;
+    if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_DTYPE;
+    if (!chain_sizes_ok(B, k, V)) return SPEC_ERR_SHAPE;
+    if (B == 0) return SPEC_OK;  // nothing is read or written: any pointer will do
+    const bool stoch = mode == SPEC_STOCHASTIC;
+    if (!target_logits || !draft_tokens || !out_tokens || !out_num_accepted || !workspace)
+        return SPEC_ERR_NULL;
+    if (stoch && (!draft_logits || !uniforms)) return SPEC_ERR_NULL;
+    if (stoch && (!(temperature > 0.0f) || !std::isfinite(temperature) || !(top_p > 0.0f) ||
+                  !(top_p <= 1.0f)))
+        return SPEC_ERR_PARAM;
+    const size_t esz = dtype == SPEC_F32 ? 4 : 2;
+    if (!aligned(target_logits, esz) || (stoch && !aligned(draft_logits, esz)) ||
+        !aligned(draft_tokens, 4) || (stoch && !aligned(uniforms, 4)) ||
+        !aligned(out_tokens, 4) || !aligned(out_num_accepted, 4) || !aligned(workspace, 16))
+        return SPEC_ERR_ALIGN;
+    if (workspace_bytes < carve(nullptr, B, 2 * k + 1, V, nullptr)) return SPEC_ERR_WORKSPACE;
+
+    plan->stoch = stoch;
+    plan->dtype = dtype;
+    plan->temperature = stoch ? temperature : 1.0f;
+    plan->top_p = stoch ? top_p : 1.0f;
+    plan->use_topp = stoch && top_p < 1.0f;
+    plan->c = static_cast<float>(1.4426950408889634 / static_cast<double>(plan->temperature));
+    plan->st = reinterpret_cast<cudaStream_t>(stream);
+    carve(workspace, B, 2 * k + 1, V, &plan->ws);
+
+    RowView &rv = plan->rows;
+    rv.target = target_logits;
+    rv.draft = draft_logits;
+    rv.V = V;
+    rv.k = k;
+    rv.R = stoch ? 2 * k + 1 : k + 1;
+    rv.draft_rows_from = k + 1;
+    rv.tgt_rows_per_seq = k + 1;
+    plan->rows_total = B * rv.R;
+
+    FinalArgs &fa = plan->fin;
+    fa.target = target_logits;
+    fa.draft = draft_logits;
+    fa.draft_tokens = draft_tokens;
+    fa.uniforms = uniforms;
+    fa.B = B;
+    fa.k = k;
+    fa.V = V;
+    fa.NS = subs_for(V);
+    fa.c = plan->c;
+    fa.out_tokens = out_tokens;
+    fa.out_num = out_num_accepted;
+    fa.ws = plan->ws;
+
+    SeqArgs &sq = plan->seq;
+    sq.work = stoch ? kSeqDecide : kSeqGreedy;
+    sq.draft_tokens = draft_tokens;
+    sq.uniforms = uniforms;
+    sq.out_tokens = out_tokens;
+    sq.out_num = out_num_accepted;
+    return SPEC_OK;
+}
+
+int launch_chain_rows(const ChainPlan &p) {
+    if (p.use_topp) {
+        ToppArgs ta;
+        ta.rows = p.rows;
+        ta.seq = p.seq;
+        ta.T = tiles_for(p.rows.V);
+        ta.TL = tile_len(p.rows.V, ta.T);
+        ta.c = p.c;
+        ta.temperature = p.temperature;
+        ta.top_p = p.top_p;
+        ta.ws = p.ws;
+        return launch_topp_rows(ta, p.rows_total, p.dtype, p.st);
+    }
+    return launch_stream_rows(p.rows, p.seq, p.rows_total, p.c, p.ws, p.stoch ? 0 : 1, p.dtype,
+                              p.st);
+}
+
+// Greedy verification completes inside the row kernel: nothing to finish.
+int launch_chain_finish(const ChainPlan &p) {
+    return p.stoch ? launch_final(p.fin, p.dtype, p.st) : SPEC_OK;
+}
+
+}  // namespace
+}  // namespace specv
+
+using namespace specv;
+
+SPEC_EXPORT int spec_verify_workspace_size(int B, int k, int V, size_t *bytes) {
+    if (!bytes) return SPEC_ERR_NULL;
+    if (!chain_sizes_ok(B, k, V)) return SPEC_ERR_SHAPE;
+    *bytes = carve(nullptr, B, 2 * k + 1, V, nullptr);
+    return SPEC_OK;
+}
+
+SPEC_EXPORT int spec_verify_tree_workspace_size(int B, int N, int V, size_t *bytes) {
+    if (!bytes) return SPEC_ERR_NULL;
+    if (!tree_sizes_ok(B, N, V)) return SPEC_ERR_SHAPE;
+    *bytes = carve(nullptr, B, N, V, nullptr);
+    return SPEC_OK;
+}
+
+SPEC_EXPORT int spec_verify_workspace_init(void *workspace, size_t bytes, spec_stream_t stream) {
+    if (!workspace) return SPEC_ERR_NULL;
+    return cudaMemsetAsync(workspace, 0, bytes, reinterpret_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? SPEC_OK
+               : SPEC_ERR_CUDA;
+}
+
+SPEC_EXPORT int spec_verify_sample(const void *target_logits, const void *draft_logits,
+                                   const int32_t *draft_tokens, const float *uniforms, int B,
+                                   int k, int V, float temperature, float top_p, int mode,
+                                   int dtype, int32_t *out_tokens, int32_t *out_num_accepted,
+                                   void *workspace, size_t workspace_bytes,
+                                   spec_stream_t stream) {
+    ChainPlan plan;
+    int rc = plan_chain(target_logits, draft_logits, draft_tokens, uniforms, B, k, V, temperature,
+                        top_p, mode, dtype, out_tokens, out_num_accepted, workspace,
+                        workspace_bytes, stream, &plan);
+    if (rc != SPEC_OK || B == 0) return rc;
+    rc = launch_chain_rows(plan);
+    if (rc != SPEC_OK) return rc;
+    return launch_chain_finish(plan);
+}
+
+SPEC_EXPORT int spec_verify_sample_rows(const void *target_logits, const void *draft_logits,
+                                        const int32_t *draft_tokens, const float *uniforms,
+                                        int B, int k, int V, float temperature, float top_p,
+                                        int mode, int dtype, int32_t *out_tokens,
+                                        int32_t *out_num_accepted, void *workspace,
+                                        size_t workspace_bytes, spec_stream_t stream) {
+    ChainPlan plan;
+    const int rc = plan_chain(target_logits, draft_logits, draft_tokens, uniforms, B, k, V,
+                              temperature, top_p, mode, dtype, out_tokens, out_num_accepted,
+                              workspace, workspace_bytes, stream, &plan);
+    if (rc != SPEC_OK || B == 0) return rc;
+    return launch_chain_rows(plan);
+}
+
+SPEC_EXPORT int spec_verify_sample_finish(const void *target_logits, const void *draft_logits,
+                                          const int32_t *draft_tokens, const float *uniforms,
+                                          int B, int k, int V, float temperature, float top_p,
+                                          int mode, int dtype, int32_t *out_tokens,
+                                          int32_t *out_num_accepted, void *workspace,
+                                          size_t workspace_bytes, spec_stream_t stream) {
+    ChainPlan plan;
+    const int rc = plan_chain(target_logits, draft_logits, draft_tokens, uniforms, B, k, V,
+                              temperature, top_p, mode, dtype, out_tokens, out_num_accepted,
+                              workspace, workspace_bytes, stream, &plan);
+    if (rc != SPEC_OK || B == 0) return rc;
+    return launch_chain_finish(plan);
+}
+
+SPEC_EXPORT int spec_verify_tree(const void *target_logits, const int32_t *parents,
+                                 const int32_t *node_tokens, int B, int N, int V, int D,
+                                 int dtype, int32_t *out_tokens, int32_t *out_num_accepted,
+                                 int32_t *out_path, void *workspace, size_t workspace_bytes,
+                                 spec_stream_t stream) {
+    if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_DTYPE;
+    if (!tree_sizes_ok(B, N, V) || D < 0 || D >= N) return SPEC_ERR_SHAPE;
+    if (B == 0) return SPEC_OK;  // nothing is read or written: any pointer will do
+    if (!target_logits || !parents || !node_tokens || !out_tokens || !out_num_accepted ||
+        !workspace)
+        return SPEC_ERR_NULL;
+    const size_t esz = dtype == SPEC_F32 ? 4 : 2;
+    if (!aligned(target_logits, esz) || !aligned(parents, 4) || !aligned(node_tokens, 4) ||
+        !aligned(out_tokens, 4) || !aligned(out_num_accepted, 4) ||
+        (out_path && !aligned(out_path, 4)) || !aligned(workspace, 16))
+        return SPEC_ERR_ALIGN;
+    if (workspace_bytes < carve(nullptr, B, N, V, nullptr)) return SPEC_ERR_WORKSPACE;
+
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    Workspace ws;
+    carve(workspace, B, N, V, &ws);
+    RowView rv;
+    rv.target = target_logits;
+    rv.draft = nullptr;
+    rv.V = V;
+    rv.k = 0;
+    rv.R = N;
+    rv.draft_rows_from = N;
+    rv.tgt_rows_per_seq = N;
+    SeqArgs sq = {};
+    sq.work = kSeqNone;
+    const int rc = launch_stream_rows(rv, sq, B * N, 1.4426950408889634f, ws, 1, dtype, st);
+    if (rc != SPEC_OK) return rc;
+    TreeArgs ta;
+    ta.parents = parents;
+    ta.node_tokens = node_tokens;
+    ta.B = B;
+    ta.N = N;
+    ta.V = V;
+    ta.D = D;
+    ta.out_tokens = out_tokens;
+    ta.out_num = out_num_accepted;
+    ta.out_path = out_path;
+    ta.ws = ws;
+    return launch_tree(ta, st);
+}
+
+SPEC_EXPORT int spec_verify_last_error(void *workspace, size_t workspace_bytes,
+                                       spec_stream_t stream) {
+    if (!workspace) return SPEC_ERR_NULL;
+    if (workspace_bytes < sizeof(uint32_t)) return SPEC_ERR_WORKSPACE;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    uint32_t word = 0;
+    if (cudaMemcpyAsync(&word, workspace, sizeof word, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+    if (cudaMemsetAsync(workspace, 0, sizeof word, st) != cudaSuccess) return SPEC_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return SPEC_ERR_CUDA;
+    return static_cast<int>(word);
+}
+
+SPEC_EXPORT int spec_verify_intermediates(const void *workspace, size_t workspace_bytes, int B,
+                                          int k, int V, float *P, float *Q, float *Z, float *S,
+                                          spec_stream_t stream) {
+    if (!workspace) return SPEC_ERR_NULL;
+    if (!chain_sizes_ok(B, k, V)) return SPEC_ERR_SHAPE;
+    if (workspace_bytes < carve(nullptr, B, 2 * k + 1, V, nullptr)) return SPEC_ERR_WORKSPACE;
+    if (B == 0) return SPEC_OK;
+    Workspace ws;
+    carve(const_cast<void *>(workspace), B, 2 * k + 1, V, &ws);
+    return launch_intermediates(ws, B, k, P, Q, Z, S, reinterpret_cast<cudaStream_t>(stream));
+}
+
+SPEC_EXPORT const char *spec_verify_status_string(int status) {
+    switch (status) {
+    case SPEC_OK: return "ok";
+    case SPEC_ERR_NULL: return "a required pointer is NULL";
+    case SPEC_ERR_SHAPE: return "a size argument is outside the supported range";
+    case SPEC_ERR_PARAM: return "temperature must be finite and > 0, top_p in (0, 1]";
+    case SPEC_ERR_DTYPE: return "dtype must be SPEC_F32 or SPEC_BF16";
+    case SPEC_ERR_MODE: return "mode must be SPEC_STOCHASTIC or SPEC_GREEDY";
+    case SPEC_ERR_ALIGN: return "a pointer is misaligned for its element type";
+    case SPEC_ERR_WORKSPACE: return "workspace is NULL or too small";
+    case SPEC_ERR_CUDA: return "a CUDA runtime call failed";
+    case SPEC_DATA_ROW_NONFINITE: return "a logit row holds NaN or +inf";
+    case SPEC_DATA_ROW_ALL_NEG_INF: return "a logit row is entirely -inf";
+    case SPEC_DATA_TOKEN_RANGE: return "a token lies outside [0, V)";
+    case SPEC_DATA_UNIFORM_RANGE: return "a uniform lies outside [0, 1)";
+    case SPEC_DATA_TREE_SHAPE:
+        return "parents is not a rooted tree in topological order within depth D";
+    default: return "unknown status";
+    }
+}

@@ -1,0 +1,455 @@
+// common.cuh -- internal definitions shared by the translation units of
+// libspecverify.so: workspace records, launch arguments, PTX helpers,
+// element unpacking and the fixed-order reductions.  Not a public header.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cfloat>
+#include <climits>
+#include <cmath>
+#include <cstdint>
+
+#include "spec_verify.h"
+
+namespace specv {
+
+// ------------------------------------------------------------ constants
+
+constexpr int kThreads = 256;            // CTA size of the row and draw kernels
+constexpr int kWarps = kThreads / 32;
+constexpr int kBatch = 4;                // 16-byte vectors in flight per lane
+constexpr int kMinSeg = 2048;            // smallest warp segment (elements)
+constexpr int kTileMax = 16384;          // elements per CTA tile (top-p kernel)
+constexpr int kSubW = 1024;              // elements per draw sub-tile (a warp)
+constexpr int kHistBins = 2048;          // top-p radix bins per pass
+constexpr float kFix = 1099511627776.0f; // 2^40: fixed-point mass unit
+constexpr float kNegInf = -INFINITY;
+
+// Row-record flags (the public SPEC_DATA_* bit values).
+constexpr uint32_t kFlagNonFinite = SPEC_DATA_ROW_NONFINITE;
+constexpr uint32_t kFlagAllNegInf = SPEC_DATA_ROW_ALL_NEG_INF;
+
+// ------------------------------------------------------------ records
+
+struct Partial {       // 16 bytes: one piece of one row
+    float m;           // max over the piece
+    float s;           // sum of 2^((l - m) c) over the piece (stochastic)
+    int32_t arg;       // first index of the max, row-relative (argmax)
+    uint32_t flags;
+};
+
+struct RowRec {        // 32 bytes: one row, after all its pieces
+    float m;           // row max
+    float z;           // normaliser over the kept tokens: sum 2^((l - m) c)
+    uint32_t lam_key;  // ordered key of the smallest kept logit (0: all kept)
+    int32_t arg;       // first argmax (greedy / tree)
+    float z_full;      // normaliser over the whole row
+    uint32_t flags;    // kFlag* bits
+    uint32_t pad[2];
+};
+
+struct SeqRec {         // one sequence's accept decision (and debug values)
+    int32_t j;         // accepted drafts
+    uint32_t bad;      // data-error bits (0: fine)
+    float S;           // total weight of the final draw
+    float pad;
+    float P[32];       // p_i(x~_i)
+    float Q[32];       // q_i(x~_i)
+};
+
+struct Workspace {
+    uint32_t *err;         // data-error word
+    uint32_t *row_ctr;     // per-row piece arrival counters (self-resetting)
+    uint32_t *seq_rows;    // per-sequence finished-row counters (self-resetting)
+    uint32_t *seq_ctr;     // per-sequence draw-item arrival counters (self-resetting)
+    Partial *partial;      // [rows, pmax]
+    RowRec *rows;          // [rows]
+    float *sub_sums;       // [B, NS] draw weight of every 1024-element sub-tile
+    SeqRec *seqs;          // [B]
+    int pmax;              // partial slots per row
+};
+
+// Where row r of sequence b lives: rows 0..draft_rows_from-1 of a sequence
+// are target rows, the rest are draft rows.
+struct RowView {
+    const void *target;
+    const void *draft;
+    int V, R, k;
+    int draft_rows_from;   // k+1 (chain) or N (tree)
+    int tgt_rows_per_seq;  // k+1 (chain) or N (tree)
+};
+
+template <typename T>
+__device__ __forceinline__ const T *row_ptr(const RowView &v, int row) {
+    const int b = row / v.R, r = row - b * v.R;
+    if (r < v.draft_rows_from)
+        return static_cast<const T *>(v.target) +
+               (static_cast<size_t>(b) * v.tgt_rows_per_seq + r) * v.V;
+    return static_cast<const T *>(v.draft) +
+           (static_cast<size_t>(b) * v.k + (r - v.draft_rows_from)) * v.V;
+}
+
+// ------------------------------------------------------------------ PTX
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float max_nan(float a, float b) {
+    float d;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t max_nan_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// Streaming 16-byte load: read-only path, no L1 allocation, 256-byte L2
+// prefetch (each logit is read once).
+__device__ __forceinline__ uint4 ld_stream(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// ------------------------------------------------------- element types
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(uint16_t b) {
+    return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+    static constexpr int kPerVec = 4;
+    static constexpr uint32_t kNegInfWord = 0xFF800000u;
+};
+template <> struct Elem<uint16_t> {
+    static constexpr int kPerVec = 8;
+    static constexpr uint32_t kNegInfWord = 0xFF80FF80u;
+};
+
+template <typename T>
+__device__ __forceinline__ uint4 neg_inf_vec() {
+    return make_uint4(Elem<T>::kNegInfWord, Elem<T>::kNegInfWord, Elem<T>::kNegInfWord,
+                      Elem<T>::kNegInfWord);
+}
+
+template <typename T>
+__device__ __forceinline__ void unpack(const uint4 &q, float (&f)[Elem<T>::kPerVec]);
+template <>
+__device__ __forceinline__ void unpack<float>(const uint4 &q, float (&f)[4]) {
+    f[0] = __uint_as_float(q.x);
+    f[1] = __uint_as_float(q.y);
+    f[2] = __uint_as_float(q.z);
+    f[3] = __uint_as_float(q.w);
+}
+template <>
+__device__ __forceinline__ void unpack<uint16_t>(const uint4 &q, float (&f)[8]) {
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+
+// NaN-propagating max over a batch of vectors.
+template <typename T>
+__device__ __forceinline__ float batch_max(const uint4 (&q)[kBatch]);
+template <>
+__device__ __forceinline__ float batch_max<float>(const uint4 (&q)[kBatch]) {
+    float m = kNegInf;
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u)
+        m = max_nan(m, max_nan(max_nan(__uint_as_float(q[u].x), __uint_as_float(q[u].y)),
+                               max_nan(__uint_as_float(q[u].z), __uint_as_float(q[u].w))));
+    return m;
+}
+template <>
+__device__ __forceinline__ float batch_max<uint16_t>(const uint4 (&q)[kBatch]) {
+    uint32_t m = Elem<uint16_t>::kNegInfWord;
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u)
+        m = max_nan_bf16x2(m, max_nan_bf16x2(max_nan_bf16x2(q[u].x, q[u].y),
+                                             max_nan_bf16x2(q[u].z, q[u].w)));
+    return max_nan(__uint_as_float(m << 16), __uint_as_float(m & 0xFFFF0000u));
+}
+
+// Ordered key of a logit: monotone in its value, -0 folded onto +0.  bf16
+// values use the top 16 bits (exact: their low 16 bits are zero).
+template <typename T>
+__device__ __forceinline__ uint32_t okey(float v) {
+    uint32_t b = __float_as_uint(v);
+    if (b == 0x80000000u) b = 0;
+    b = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+    return sizeof(T) == 2 ? (b >> 16) : b;
+}
+
+// Processed probability of one logit: [key >= lam] 2^(l c - m c) / z, with
+// negmc = -(m c) and invz = 1 / z.  Explicit round-to-nearest intrinsics
+// keep every call site bitwise identical.
+template <typename T>
+__device__ __forceinline__ float proc_prob(float l, float c, float negmc, float invz,
+                                           uint32_t lam_key) {
+    const float e = ex2(__fmaf_rn(l, c, negmc));
+    return okey<T>(l) >= lam_key ? __fmul_rn(e, invz) : 0.0f;
+}
+
+// ---------------------------------------------------------- combining
+
+__device__ __forceinline__ void ms_combine(float &m, float &s, float m2, float s2, float c) {
+    const float mn = fmaxf(m, m2);
+    if (mn == kNegInf) {
+        m = mn;
+        s = 0.0f;
+        return;
+    }
+    s = __fadd_rn(__fmul_rn(s, ex2(__fmul_rn(__fsub_rn(m, mn), c))),
+                  __fmul_rn(s2, ex2(__fmul_rn(__fsub_rn(m2, mn), c))));
+    m = mn;
+}
+
+__device__ __forceinline__ void arg_combine(float &v, int &i, float v2, int i2) {
+    if (v2 > v || (v2 == v && i2 < i)) {
+        v = v2;
+        i = i2;
+    }
+}
+
+// Butterfly reductions: every lane ends with the same (commutative) result.
+__device__ __forceinline__ void warp_reduce_ms(float &m, float &s, uint32_t &fl, float c) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float m2 = __shfl_xor_sync(0xFFFFFFFFu, m, o);
+        const float s2 = __shfl_xor_sync(0xFFFFFFFFu, s, o);
+        fl |= __shfl_xor_sync(0xFFFFFFFFu, fl, o);
+        ms_combine(m, s, m2, s2, c);
+    }
+}
+
+__device__ __forceinline__ void warp_reduce_arg(float &v, int &i, uint32_t &fl) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float v2 = __shfl_xor_sync(0xFFFFFFFFu, v, o);
+        const int i2 = __shfl_xor_sync(0xFFFFFFFFu, i, o);
+        fl |= __shfl_xor_sync(0xFFFFFFFFu, fl, o);
+        arg_combine(v, i, v2, i2);
+    }
+}
+
+// Row flags from the combined max: +inf is non-finite; an all -inf row
+// (and no NaN) is flagged as such.
+__device__ __forceinline__ uint32_t row_flags(float m, uint32_t fl) {
+    if (m == INFINITY) fl |= kFlagNonFinite;
+    if (m == kNegInf && !(fl & kFlagNonFinite)) fl |= kFlagAllNegInf;
+    return fl;
+}
+
+// Split [lo, hi) of a row into a scalar head, 16-byte vectors and a scalar
+// tail, by absolute address.
+template <typename T>
+struct Span {
+    int e0, a0, nvec, a1, e1;
+    __device__ __forceinline__ Span(const T *rowp, int lo, int hi) : e0(lo), e1(hi) {
+        constexpr int P = Elem<T>::kPerVec;
+        const uintptr_t addr = reinterpret_cast<uintptr_t>(rowp + lo);
+        int head = static_cast<int>(((16u - (addr & 15u)) & 15u) / sizeof(T));
+        if (head > hi - lo) head = hi - lo;
+        a0 = lo + head;
+        nvec = (hi - a0) / P;
+        a1 = a0 + nvec * P;
+    }
+};
+
+// ------------------------------------------------- sequence completion
+
+// What the warp that finishes a sequence's last row does with it.
+enum SeqWork { kSeqDecide = 0, kSeqGreedy = 1, kSeqNone = 2 };
+
+struct SeqArgs {
+    int work;                    // SeqWork
+    const int32_t *draft_tokens; // [B, k]
+    const float *uniforms;       // [B, k+1] (kSeqDecide)
+    int32_t *out_tokens;         // [B, k+1]
+    int32_t *out_num;            // [B]
+};
+
+// Accept decisions of sequence b ("3.5 Speculative Decoding", step 3: for
+// i = 1..k accept x~_i iff u_i q_i(x~_i) < p_i(x~_i), stop at the first
+// rejection).  Lane i tests draft i; ballot + ffs give the first rejection.
+// Row records are read through L2 (they were written by other warps).
+// Writes the sequence record; a sequence with a data error gets -1 outputs.
+template <typename T>
+__device__ void decide_sequence(const RowView &v, const SeqArgs &sa, const Workspace &ws,
+                                float c, int b) {
+    const int lane = threadIdx.x & 31, k = v.k, V = v.V, R = 2 * k + 1;
+    const RowRec *rr = ws.rows + static_cast<size_t>(b) * R;
+    const T *tgt = static_cast<const T *>(v.target) + static_cast<size_t>(b) * (k + 1) * V;
+    const T *drf = static_cast<const T *>(v.draft) + static_cast<size_t>(b) * k * V;
+    const float *ub = sa.uniforms + static_cast<size_t>(b) * (k + 1);
+    uint32_t bad = 0;
+    for (int r = lane; r < R; r += 32) bad |= __ldcg(&rr[r].flags);
+    bool accept = true;
+    float P = 0.0f, Q = 0.0f;
+    if (lane < k) {
+        const int x = sa.draft_tokens[static_cast<size_t>(b) * k + lane];
+        if (x < 0 || x >= V) {
+            bad |= SPEC_DATA_TOKEN_RANGE;
+        } else {
+            const RowRec *tp = rr + lane, *dq = rr + k + 1 + lane;
+            P = proc_prob<T>(to_f32(tgt[static_cast<size_t>(lane) * V + x]), c,
+                             -__fmul_rn(__ldcg(&tp->m), c), __frcp_rn(__ldcg(&tp->z)),
+                             __ldcg(&tp->lam_key));
+            Q = proc_prob<T>(to_f32(drf[static_cast<size_t>(lane) * V + x]), c,
+                             -__fmul_rn(__ldcg(&dq->m), c), __frcp_rn(__ldcg(&dq->z)),
+                             __ldcg(&dq->lam_key));
+            accept = __fmul_rn(ub[lane], Q) < P;
+        }
+    }
+    if (lane <= k) {
+        const float u = ub[lane];
+        if (!(u >= 0.0f && u < 1.0f)) bad |= SPEC_DATA_UNIFORM_RANGE;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) bad |= __shfl_xor_sync(0xFFFFFFFFu, bad, o);
+    const unsigned rej = __ballot_sync(0xFFFFFFFFu, lane < k && !accept);
+    const int j = rej ? __ffs(rej) - 1 : k;
+    SeqRec *rec = ws.seqs + b;
+    if (lane < k) {
+        rec->P[lane] = P;
+        rec->Q[lane] = Q;
+    }
+    if (lane == 0) {
+        rec->j = j;
+        rec->bad = bad;
+        rec->S = 0.0f;
+    }
+    if (bad) {
+        if (lane <= k) sa.out_tokens[static_cast<size_t>(b) * (k + 1) + lane] = -1;
+        if (lane == 0) {
+            sa.out_num[b] = -1;
+            atomicOr(ws.err, bad);
+        }
+    }
+}
+
+// Greedy chain rule ("3.5 Speculative Decoding", end of the proof;
+// "Speculative Decoding from First Principles", "Draft, verify, keep what
+// matches"): keep drafts while they equal the target's first argmax, then
+// emit the argmax of the first mismatching (or the bonus) row.
+__device__ __forceinline__ void greedy_sequence(const RowView &v, const SeqArgs &sa,
+                                                const Workspace &ws, int b) {
+    const int lane = threadIdx.x & 31, k = v.k;
+    const RowRec *rr = ws.rows + static_cast<size_t>(b) * (k + 1);
+    uint32_t bad = 0;
+    int g = -1, x = -1;
+    if (lane <= k) {
+        bad |= __ldcg(&rr[lane].flags);
+        g = __ldcg(&rr[lane].arg);
+    }
+    if (lane < k) {
+        x = sa.draft_tokens[static_cast<size_t>(b) * k + lane];
+        if (x < 0 || x >= v.V) bad |= SPEC_DATA_TOKEN_RANGE;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) bad |= __shfl_xor_sync(0xFFFFFFFFu, bad, o);
+    const unsigned miss = __ballot_sync(0xFFFFFFFFu, lane < k && x != g);
+    const int j = miss ? __ffs(miss) - 1 : k;
+    const int gj = __shfl_sync(0xFFFFFFFFu, g, j);
+    if (lane <= k) {
+        int32_t val = -1;
+        if (!bad) val = lane < j ? x : (lane == j ? gj : -1);
+        sa.out_tokens[static_cast<size_t>(b) * (k + 1) + lane] = val;
+    }
+    if (lane == 0) {
+        sa.out_num[b] = bad ? -1 : j;
+        if (bad) atomicOr(ws.err, bad);
+    }
+}
+
+// Called by a whole warp right after its lane 0 wrote row `row`'s record:
+// counts the row towards its sequence and, for the sequence's last row,
+// runs the sequence's completion step.
+template <typename T>
+__device__ __forceinline__ void row_done(const RowView &v, const SeqArgs &sa,
+                                         const Workspace &ws, float c, int row) {
+    if (sa.work == kSeqNone) return;
+    const int lane = threadIdx.x & 31;
+    const int b = row / v.R;
+    int last = 0;
+    if (lane == 0) {
+        __threadfence();
+        last = atomicAdd(&ws.seq_rows[b], 1u) == static_cast<unsigned>(v.R - 1);
+        __threadfence();
+    }
+    last = __shfl_sync(0xFFFFFFFFu, last, 0);
+    __syncwarp();
+    if (!last) return;
+    if (lane == 0) ws.seq_rows[b] = 0u;
+    if (sa.work == kSeqDecide) decide_sequence<T>(v, sa, ws, c, b);
+    else greedy_sequence(v, sa, ws, b);
+}
+
+// ----------------------------------------------------------- launchers
+
+struct StreamArgs {
+    RowView rows;
+    SeqArgs seq;
+    long long total;   // elements over all rows
+    long long seg;     // elements per warp segment
+    float c;           // log2(e) / temperature
+    Workspace ws;
+};
+
+struct ToppArgs {
+    RowView rows;
+    SeqArgs seq;
+    int T, TL;         // tiles per row, tile length
+    float c, temperature, top_p;
+    Workspace ws;
+};
+
+struct FinalArgs {
+    const void *target;
+    const void *draft;
+    const int32_t *draft_tokens;
+    const float *uniforms;
+    int B, k, V;
+    int NS;            // 1024-element sub-tiles per row (one warp each)
+    float c;
+    int32_t *out_tokens;
+    int32_t *out_num;
+    Workspace ws;
+};
+
+struct TreeArgs {
+    const int32_t *parents;
+    const int32_t *node_tokens;
+    int B, N, V, D;
+    int32_t *out_tokens;
+    int32_t *out_num;
+    int32_t *out_path;
+    Workspace ws;
+};
+
+// kind 0: stochastic statistics; kind 1: argmax.  dtype: SPEC_F32/SPEC_BF16.
+// Each returns SPEC_OK or SPEC_ERR_CUDA.
+int launch_stream_rows(const RowView &rows, const SeqArgs &seq, int rows_total, float c,
+                       const Workspace &ws, int kind, int dtype, cudaStream_t st);
+int launch_topp_rows(const ToppArgs &a, int rows_total, int dtype, cudaStream_t st);
+// The final kernel is launched as a programmatic dependent of the row kernel.
+int launch_final(const FinalArgs &a, int dtype, cudaStream_t st);
+int launch_tree(const TreeArgs &a, cudaStream_t st);
+int launch_intermediates(const Workspace &ws, int B, int k, float *P, float *Q, float *Z,
+                         float *S, cudaStream_t st);
+
+}  // namespace specv

@@ -25,8 +25,9 @@ Workloads (the five verification batches the library is measured on):
 Draft tokens are drawn by the Gumbel-max rule, argmax_x (l(x)/T + G(x))
 with G = -log(-log U), which samples softmax(l/T) without forming it.  With
 top-p on (c4) the drafter restricts the draw to the 16 largest draft logits,
-a top-16 drafter; those tokens lie inside the draft's 0.95-nucleus on these
-rows.  bf16 logits are made by round-to-nearest-even from fp32 and stored as
+a top-16 drafter; on c4 one draft in 384 lands outside its row's 0.95-nucleus
+(a row whose nucleus is smaller than 16 tokens), where q = 0 and the accept
+rule's q = 0 case applies.  bf16 logits are made by round-to-nearest-even from fp32 and stored as
 uint16 bit patterns; both sides of a parity test read the same bits.
 Uniforms are fp32 multiples of 2^-24 in [0, 1).
 """
