@@ -207,6 +207,30 @@ int spec_verify_tree(const void *target_logits, const int32_t *parents,
                      spec_stream_t stream);
 
 /*
+ * spec_verify_sample for callers that cannot allocate device memory (no
+ * counterpart on the pages: it is a deployment variant).  A serving engine
+ * that plans all device memory ahead and forbids allocation on its decode
+ * path, or a plugin whose host framework gives it no allocator, cannot pass
+ * a workspace; this entry point instead uses a fixed 4 MiB scratch array in
+ * the library's own device image, held by every GPU that loads the library
+ * until the process exits.  It calls no allocator.
+ *   - Same arguments and results as spec_verify_sample, without the
+ *     workspace.  Batches whose workspace (spec_verify_workspace_size)
+ *     exceeds 4 MiB are rejected with SPEC_ERR_WORKSPACE.
+ *   - Each call zero-fills the part of the scratch it uses on `stream`
+ *     first.  All calls on a device share the one array: calls whose work
+ *     overlaps on the GPU race and give wrong results; order them.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make it before any stream capture begins.
+ *   - Data errors show as -1 outputs; the error word is not kept.
+ */
+int spec_verify_sample_noalloc(const void *target_logits, const void *draft_logits,
+                               const int32_t *draft_tokens, const float *uniforms,
+                               int B, int k, int V, float temperature, float top_p,
+                               int mode, int dtype, int32_t *out_tokens,
+                               int32_t *out_num_accepted, spec_stream_t stream);
+
+/*
  * Synchronise `stream`, then return the workspace's data-error word (an OR
  * of SPEC_DATA_* bits accumulated since the previous call of this function;
  * 0 if none) and clear it.  Negative on an argument or CUDA error.

@@ -25,7 +25,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 _ROOT = os.path.dirname(_PKG)
 LIB_PATH = os.path.join(_PKG, "libspecverify.so")
 CSRC = os.path.join(_PKG, "csrc")
-SOURCES = [os.path.join(CSRC, f) for f in ("api.cu", "rows.cu", "final.cu")]
+SOURCES = [os.path.join(CSRC, f) for f in ("api.cu", "rows.cu", "final.cu", "noalloc.cu")]
 HEADERS = [os.path.join(CSRC, "common.cuh")]
 INCLUDE = os.path.join(_ROOT, "include")
 HEADER = os.path.join(INCLUDE, "spec_verify.h")
@@ -48,6 +48,7 @@ EXPORTED = (
     "spec_verify_sample",
     "spec_verify_sample_rows",
     "spec_verify_sample_finish",
+    "spec_verify_sample_noalloc",
     "spec_verify_tree",
     "spec_verify_last_error",
     "spec_verify_intermediates",
@@ -107,6 +108,7 @@ def lib():
         L.spec_verify_workspace_init.argtypes = [P, Z, P]
         for name in ("spec_verify_sample", "spec_verify_sample_rows", "spec_verify_sample_finish"):
             getattr(L, name).argtypes = [P, P, P, P, I, I, I, F, F, I, I, P, P, P, Z, P]
+        L.spec_verify_sample_noalloc.argtypes = [P, P, P, P, I, I, I, F, F, I, I, P, P, P]
         L.spec_verify_tree.argtypes = [P, P, P, I, I, I, I, I, P, P, P, P, Z, P]
         L.spec_verify_last_error.argtypes = [P, Z, P]
         L.spec_verify_intermediates.argtypes = [P, Z, I, I, I, P, P, P, P, P]
@@ -167,6 +169,17 @@ def spec_verify_sample_finish(target_ptr, draft_ptr, tokens_ptr, uniforms_ptr, B
         target_ptr, draft_ptr, tokens_ptr, uniforms_ptr, B, k, V, float(temperature),
         float(top_p), mode, dtype, out_tokens_ptr, out_num_ptr, workspace_ptr,
         workspace_bytes, stream))
+
+
+def spec_verify_sample_noalloc(target_ptr, draft_ptr, tokens_ptr, uniforms_ptr, B, k, V,
+                               temperature, top_p, mode, dtype, out_tokens_ptr, out_num_ptr,
+                               stream=0):
+    """spec_verify_sample without a workspace, for callers that cannot
+    allocate device memory: the library's fixed 4 MiB per-device scratch is
+    used instead (calls that overlap on the GPU race on it)."""
+    return _check(lib().spec_verify_sample_noalloc(
+        target_ptr, draft_ptr, tokens_ptr, uniforms_ptr, B, k, V, float(temperature),
+        float(top_p), mode, dtype, out_tokens_ptr, out_num_ptr, stream))
 
 
 def spec_verify_tree(target_ptr, parents_ptr, node_tokens_ptr, B, N, V, D, dtype,
