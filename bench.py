@@ -42,7 +42,7 @@ import workloads  # noqa: E402
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 7900.0
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "rows_kernel_c3.md")
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "stream_kernel_c3.md")
 KERNEL_SOURCES = [os.path.join(ROOT, "speculative_decoding_verification_top_gb300", "csrc", f)
                   for f in ("common.cuh", "rows.cu")]
 
@@ -379,14 +379,14 @@ def run_ours(args):
 
     if rows_ms is not None:
         achieved = nbytes / (rows_ms * 1e-3) / 1e9
-        roofline = {"bound": "hbm", "kernel": "rows_kernel", "achieved": round(achieved, 1),
+        roofline = {"bound": "hbm", "kernel": "stream_kernel", "achieved": round(achieved, 1),
                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                     "frac": round(achieved / peak, 4), "traffic": profiled_traffic(),
                     "algorithmic_bytes": nbytes, "avg_launch_us": round(rows_ms * 1e3, 2)}
     else:
         per_launch_ms = ms_step  # the tree call: argmax rows kernel dominates
         achieved = nbytes / (per_launch_ms * 1e-3) / 1e9
-        roofline = {"bound": "hbm", "kernel": "rows_kernel+tree_kernel", "achieved": round(achieved, 1),
+        roofline = {"bound": "hbm", "kernel": "stream_kernel+tree_kernel", "achieved": round(achieved, 1),
                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                     "frac": round(achieved / peak, 4), "traffic": None,
                     "algorithmic_bytes": nbytes, "avg_launch_us": round(per_launch_ms * 1e3, 2)}

@@ -53,7 +53,11 @@ struct SeqRec {         // one sequence's accept decision (and debug values)
     int32_t j;         // accepted drafts
     uint32_t bad;      // data-error bits (0: fine)
     float S;           // total weight of the final draw
-    float pad;
+    uint32_t use_p;    // draw from p_{j+1} (bonus row) instead of the residual
+    float pneg, pinv;  // -(m c) and 1/z of the draw's target row
+    float qneg, qinv;  // the same for the draft row (residual only)
+    uint32_t plam, qlam;  // nucleus keys of the two rows
+    float pad[2];
     float P[32];       // p_i(x~_i)
     float Q[32];       // q_i(x~_i)
 };
@@ -108,6 +112,16 @@ __device__ __forceinline__ uint32_t max_nan_bf16x2(uint32_t a, uint32_t b) {
     uint32_t d;
     asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
     return d;
+}
+
+// Atomic add with acquire-release semantics at GPU scope: the calling
+// thread's earlier writes are visible to whoever observes the new count,
+// and writes released by earlier arrivals are visible to this thread after
+// it.  Returns the old value.
+__device__ __forceinline__ unsigned arrive(unsigned *ctr, unsigned n) {
+    unsigned old;
+    asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], %2;" : "=r"(old) : "l"(ctr), "r"(n) : "memory");
+    return old;
 }
 
 // Streaming 16-byte load: read-only path, no L1 allocation, 256-byte L2
@@ -329,9 +343,20 @@ __device__ void decide_sequence(const RowView &v, const SeqArgs &sa, const Works
         rec->Q[lane] = Q;
     }
     if (lane == 0) {
+        // The final draw's rows: target row j and draft row j (residual), or
+        // the bonus target row k.
+        const RowRec *pr = rr + j;
+        const RowRec *qr = j < k ? rr + k + 1 + j : pr;
         rec->j = j;
         rec->bad = bad;
         rec->S = 0.0f;
+        rec->use_p = j == k;
+        rec->pneg = -__fmul_rn(__ldcg(&pr->m), c);
+        rec->pinv = __frcp_rn(__ldcg(&pr->z));
+        rec->plam = __ldcg(&pr->lam_key);
+        rec->qneg = -__fmul_rn(__ldcg(&qr->m), c);
+        rec->qinv = __frcp_rn(__ldcg(&qr->z));
+        rec->qlam = __ldcg(&qr->lam_key);
     }
     if (bad) {
         if (lane <= k) sa.out_tokens[static_cast<size_t>(b) * (k + 1) + lane] = -1;
@@ -386,11 +411,7 @@ __device__ __forceinline__ void row_done(const RowView &v, const SeqArgs &sa,
     const int lane = threadIdx.x & 31;
     const int b = row / v.R;
     int last = 0;
-    if (lane == 0) {
-        __threadfence();
-        last = atomicAdd(&ws.seq_rows[b], 1u) == static_cast<unsigned>(v.R - 1);
-        __threadfence();
-    }
+    if (lane == 0) last = arrive(&ws.seq_rows[b], 1u) == static_cast<unsigned>(v.R - 1);
     last = __shfl_sync(0xFFFFFFFFu, last, 0);
     __syncwarp();
     if (!last) return;
@@ -424,7 +445,8 @@ struct FinalArgs {
     const int32_t *draft_tokens;
     const float *uniforms;
     int B, k, V;
-    int NS;            // 1024-element sub-tiles per row (one warp each)
+    int NS;            // 1024-element sub-tiles per row
+    long long per;     // sub-tiles per warp (contiguous run in (b, t) order)
     float c;
     int32_t *out_tokens;
     int32_t *out_num;
@@ -440,6 +462,28 @@ struct TreeArgs {
     int32_t *out_path;
     Workspace ws;
 };
+
+// Resident CTAs of `kernel` (kThreads threads) on the current device,
+// cached per device and `slot`; 0 on a CUDA error.
+template <typename K>
+int resident_ctas(K kernel, int slot) {
+    constexpr int kMaxDev = 64, kSlots = 8;
+    static int cache[kMaxDev][kSlots];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev || slot < 0 ||
+        slot >= kSlots)
+        return 0;
+    int v = __atomic_load_n(&cache[dev][slot], __ATOMIC_RELAXED);
+    if (v > 0) return v;
+    int sms = 0, per_sm = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0) !=
+            cudaSuccess)
+        return 0;
+    v = sms * (per_sm > 0 ? per_sm : 1);
+    __atomic_store_n(&cache[dev][slot], v, __ATOMIC_RELAXED);
+    return v;
+}
 
 // kind 0: stochastic statistics; kind 1: argmax.  dtype: SPEC_F32/SPEC_BF16.
 // Each returns SPEC_OK or SPEC_ERR_CUDA.

@@ -28,42 +28,61 @@ struct Draw {
     uint32_t plam, qlam;
     bool use_p;  // weights p (bonus row, or empty residual) instead of max(0, p - q)
     bool vec;    // both rows 16-byte aligned: vector loads
+    bool masked; // a nucleus threshold is set (top-p): test each logit's key
 };
 
+// The draw of sequence b, from the parameters its decider stored.
 template <typename T>
-__device__ __forceinline__ Draw<T> make_draw(const FinalArgs &a, int b, int j) {
-    const int k = a.k, V = a.V, R = 2 * k + 1;
-    const RowRec *rr = a.ws.rows + static_cast<size_t>(b) * R;
+__device__ __forceinline__ Draw<T> make_draw(const FinalArgs &a, int b, const SeqRec *rec) {
+    const int k = a.k, V = a.V;
+    const int j = __ldcg(&rec->j);
     Draw<T> d;
-    d.use_p = j == k;
+    d.use_p = __ldcg(&rec->use_p) != 0;
     d.prow = static_cast<const T *>(a.target) + (static_cast<size_t>(b) * (k + 1) + j) * V;
     d.qrow = d.use_p ? d.prow
                      : static_cast<const T *>(a.draft) + (static_cast<size_t>(b) * k + j) * V;
-    const RowRec pr = rr[j];
-    const RowRec qr = d.use_p ? pr : rr[k + 1 + j];
-    d.pneg = -__fmul_rn(pr.m, a.c);
-    d.pinv = __frcp_rn(pr.z);
-    d.plam = pr.lam_key;
-    d.qneg = -__fmul_rn(qr.m, a.c);
-    d.qinv = __frcp_rn(qr.z);
-    d.qlam = qr.lam_key;
+    d.pneg = __ldcg(&rec->pneg);
+    d.pinv = __ldcg(&rec->pinv);
+    d.plam = __ldcg(&rec->plam);
+    d.qneg = __ldcg(&rec->qneg);
+    d.qinv = __ldcg(&rec->qinv);
+    d.qlam = __ldcg(&rec->qlam);
     d.vec = (reinterpret_cast<uintptr_t>(d.prow) & 15u) == 0 &&
             (reinterpret_cast<uintptr_t>(d.qrow) & 15u) == 0;
+    d.masked = d.plam != 0u || d.qlam != 0u;
     return d;
 }
 
-// Load the VE logits of one row starting at element x (x a multiple of VE);
-// elements at or beyond V read as -inf.
+// The raw 16-byte vector of VE logits of one row starting at element x (x a
+// multiple of VE); elements at or beyond V read as -inf.
+template <typename T>
+__device__ __forceinline__ uint4 load_raw(const T *row, int x, int V, bool vec) {
+    constexpr int VE = Elem<T>::kPerVec;
+    if (vec && x + VE <= V) return __ldg(reinterpret_cast<const uint4 *>(row + x));
+    uint32_t w[4];
+    if (sizeof(T) == 4) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            w[e] = x + e < V ? __float_as_uint(to_f32(row[x + e])) : Elem<float>::kNegInfWord;
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t lo = x + 2 * i < V ? __float_as_uint(to_f32(row[x + 2 * i])) >> 16
+                                              : 0xFF80u;
+            const uint32_t hi = x + 2 * i + 1 < V
+                                    ? __float_as_uint(to_f32(row[x + 2 * i + 1])) >> 16
+                                    : 0xFF80u;
+            w[i] = lo | (hi << 16);
+        }
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Load the VE logits of one row starting at element x as floats.
 template <typename T>
 __device__ __forceinline__ void load_run(const T *row, int x, int V, bool vec,
                                          float (&f)[Elem<T>::kPerVec]) {
-    constexpr int VE = Elem<T>::kPerVec;
-    if (vec && x + VE <= V) {
-        unpack<T>(__ldg(reinterpret_cast<const uint4 *>(row + x)), f);
-    } else {
-#pragma unroll
-        for (int e = 0; e < VE; ++e) f[e] = x + e < V ? to_f32(row[x + e]) : kNegInf;
-    }
+    unpack<T>(load_raw<T>(row, x, V, vec), f);
 }
 
 // Draw weights of the VE elements starting at x from their loaded logits.
@@ -73,6 +92,23 @@ __device__ __forceinline__ void weights_from(const Draw<T> &d, int x, int V, flo
                                              const float (&lq)[Elem<T>::kPerVec],
                                              float (&w)[Elem<T>::kPerVec]) {
     constexpr int VE = Elem<T>::kPerVec;
+    if (!d.masked) {
+        // No nucleus: every logit is kept.  Residual max(0, p - q) with the
+        // subtraction folded into one fused multiply-add.
+#pragma unroll
+        for (int e = 0; e < VE; ++e) {
+            const float ep = ex2(__fmaf_rn(lp[e], c, d.pneg));
+            float wv;
+            if (d.use_p) {
+                wv = __fmul_rn(ep, d.pinv);
+            } else {
+                const float q = __fmul_rn(ex2(__fmaf_rn(lq[e], c, d.qneg)), d.qinv);
+                wv = fmaxf(__fmaf_rn(ep, d.pinv, -q), 0.0f);
+            }
+            w[e] = x + e < V ? wv : 0.0f;
+        }
+        return;
+    }
 #pragma unroll
     for (int e = 0; e < VE; ++e) {
         const float p = proc_prob<T>(lp[e], c, d.pneg, d.pinv, d.plam);
@@ -120,22 +156,24 @@ __device__ __forceinline__ int sub_x(int t, int u, int lane) {
 }
 
 // Total draw weight of sub-tile t: rounds folded in order.  All of the
-// sub-tile's loads are issued before any arithmetic.
+// sub-tile's loads are issued (as raw vectors) before any arithmetic.
 template <typename T>
 __device__ float subtile_total(const Draw<T> &d, int t, int V, float c) {
     constexpr int VE = Elem<T>::kPerVec, ROUNDS = kSubW / (32 * VE);
     const int lane = threadIdx.x & 31;
-    float lp[ROUNDS][VE], lq[ROUNDS][VE];
+    uint4 rp[ROUNDS], rq[ROUNDS];
 #pragma unroll
     for (int u = 0; u < ROUNDS; ++u) {
-        load_run<T>(d.prow, sub_x<T>(t, u, lane), V, d.vec, lp[u]);
-        if (!d.use_p) load_run<T>(d.qrow, sub_x<T>(t, u, lane), V, d.vec, lq[u]);
+        rp[u] = load_raw<T>(d.prow, sub_x<T>(t, u, lane), V, d.vec);
+        rq[u] = d.use_p ? rp[u] : load_raw<T>(d.qrow, sub_x<T>(t, u, lane), V, d.vec);
     }
     float total = 0.0f;
 #pragma unroll
     for (int u = 0; u < ROUNDS; ++u) {
-        float w[VE];
-        weights_from<T>(d, sub_x<T>(t, u, lane), V, c, lp[u], lq[u], w);
+        float lp[VE], lq[VE], w[VE];
+        unpack<T>(rp[u], lp);
+        unpack<T>(rq[u], lq);
+        weights_from<T>(d, sub_x<T>(t, u, lane), V, c, lp, lq, w);
         float v = 0.0f;
 #pragma unroll
         for (int e = 0; e < VE; ++e) v = __fadd_rn(v, w[e]);
@@ -238,41 +276,14 @@ __device__ Pick pick_subtile(const float *sums, int NS, float u) {
     return p;
 }
 
+// Last arrival for sequence b: choose the sub-tile holding u * S, scan it
+// for the token and emit the sequence's outputs.
 template <typename T>
-__global__ void __launch_bounds__(kThreads) final_kernel(const FinalArgs a) {
-    // Wait until the row kernel has finished and its writes are visible.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int lane = threadIdx.x & 31;
-    const long long wid = static_cast<long long>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
-    if (wid >= static_cast<long long>(a.B) * a.NS) return;
-    const int b = static_cast<int>(wid / a.NS);
-    const int t = static_cast<int>(wid - static_cast<long long>(b) * a.NS);
-    const int k = a.k, V = a.V;
+__device__ void finish_sequence(const FinalArgs &a, int b, Draw<T> d) {
+    const int lane = threadIdx.x & 31, k = a.k, V = a.V;
     SeqRec *rec = a.ws.seqs + b;
-    if (rec->bad) return;  // outputs already set to -1 by the row kernel
-    const int j = rec->j;
-    Draw<T> d = make_draw<T>(a, b, j);
     float *sums = a.ws.sub_sums + static_cast<size_t>(b) * a.NS;
-    const float tot = subtile_total<T>(d, t, V, a.c);
-    if (a.NS > 1) {
-        int last = 0;
-        if (lane == 0) {
-            sums[t] = tot;
-            __threadfence();
-            last = atomicAdd(&a.ws.seq_ctr[b], 1u) == static_cast<unsigned>(a.NS - 1);
-            __threadfence();
-        }
-        last = __shfl_sync(0xFFFFFFFFu, last, 0);
-        __syncwarp();
-        if (!last) return;
-        if (lane == 0) a.ws.seq_ctr[b] = 0u;
-    } else {
-        if (lane == 0) sums[0] = tot;
-        __threadfence();
-        __syncwarp();
-    }
-
-    // Last warp of the sequence: choose the sub-tile, then the token.
+    if (lane == 0) a.ws.seq_ctr[b] = 0u;
     const float u = a.uniforms[static_cast<size_t>(b) * (k + 1) + k];
     Pick pk = pick_subtile(sums, a.NS, u);
     if (!(pk.S > 0.0f) && !d.use_p) {
@@ -288,7 +299,7 @@ __global__ void __launch_bounds__(kThreads) final_kernel(const FinalArgs a) {
         pk = pick_subtile(sums, a.NS, u);
     }
     const int tok = subtile_find<T>(d, pk.t, V, a.c, pk.pre, pk.target);
-
+    const int j = __ldcg(&rec->j);
     int32_t *ot = a.out_tokens + static_cast<size_t>(b) * (k + 1);
     if (lane <= k) {
         int32_t v = -1;
@@ -299,6 +310,43 @@ __global__ void __launch_bounds__(kThreads) final_kernel(const FinalArgs a) {
     if (lane == 0) {
         a.out_num[b] = j;
         rec->S = pk.S;
+    }
+}
+
+// Persistent grid: warp w sums the sub-tiles [w per, (w+1) per) of the
+// flattened (sequence, sub-tile) order, and reports them once per sequence.
+template <typename T>
+__global__ void __launch_bounds__(kThreads, sizeof(T) == 2 ? 3 : 2) final_kernel(const FinalArgs a) {
+    // Wait until the row kernel has finished and its writes are visible.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int lane = threadIdx.x & 31;
+    const long long w = static_cast<long long>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+    const long long total = static_cast<long long>(a.B) * a.NS;
+    const long long i0 = w * a.per;
+    const long long i1 = i0 + a.per < total ? i0 + a.per : total;
+    long long i = i0;
+    while (i < i1) {
+        const int b = static_cast<int>(i / a.NS);
+        const int t0 = static_cast<int>(i - static_cast<long long>(b) * a.NS);
+        const int t1 = static_cast<int>(i1 - static_cast<long long>(b) * a.NS < a.NS
+                                            ? i1 - static_cast<long long>(b) * a.NS
+                                            : a.NS);
+        i += t1 - t0;
+        const SeqRec *rec = a.ws.seqs + b;
+        if (__ldcg(&rec->bad)) continue;  // outputs already -1 (row kernel)
+        const Draw<T> d = make_draw<T>(a, b, rec);
+        float *sums = a.ws.sub_sums + static_cast<size_t>(b) * a.NS;
+        for (int t = t0; t < t1; ++t) {
+            const float tot = subtile_total<T>(d, t, a.V, a.c);
+            if (lane == 0) sums[t] = tot;
+        }
+        int last = 0;
+        if (lane == 0)
+            last = arrive(&a.ws.seq_ctr[b], static_cast<unsigned>(t1 - t0)) + (t1 - t0) ==
+                   static_cast<unsigned>(a.NS);
+        last = __shfl_sync(0xFFFFFFFFu, last, 0);
+        __syncwarp();
+        if (last) finish_sequence<T>(a, b, d);
     }
 }
 
@@ -400,10 +448,17 @@ int status() { return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUD
 
 }  // namespace
 
-int launch_final(const FinalArgs &a, int dtype, cudaStream_t st) {
-    const long long warps = static_cast<long long>(a.B) * a.NS;
+int launch_final(const FinalArgs &in, int dtype, cudaStream_t st) {
+    FinalArgs a = in;
+    const int ctas = dtype == SPEC_F32 ? resident_ctas(final_kernel<float>, 4)
+                                       : resident_ctas(final_kernel<uint16_t>, 5);
+    if (ctas <= 0) return SPEC_ERR_CUDA;
+    const long long total = static_cast<long long>(a.B) * a.NS;
+    const long long warps = static_cast<long long>(ctas) * kWarps;
+    a.per = (total + warps - 1) / warps;
+    const long long used = (total + a.per - 1) / a.per;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>((warps + kWarps - 1) / kWarps));
+    cfg.gridDim = dim3(static_cast<unsigned>((used + kWarps - 1) / kWarps));
     cfg.blockDim = dim3(kThreads);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];

@@ -21,9 +21,6 @@
 //                 row also selects the top-p threshold from the L2-resident
 //                 row.
 
-#include <atomic>
-#include <mutex>
-
 #include "common.cuh"
 
 namespace specv {
@@ -212,9 +209,7 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(const StreamArgs a) {
                 p.arg = arg;
                 p.flags = fl;
                 a.ws.partial[static_cast<size_t>(row) * a.ws.pmax + (w - wf)] = p;
-                __threadfence();
-                last = atomicAdd(&a.ws.row_ctr[row], 1u) == static_cast<unsigned>(pieces - 1);
-                __threadfence();
+                last = arrive(&a.ws.row_ctr[row], 1u) == static_cast<unsigned>(pieces - 1);
             }
             last = __shfl_sync(0xFFFFFFFFu, last, 0);
             __syncwarp();
@@ -475,25 +470,6 @@ __global__ void __launch_bounds__(kThreads, 4) topp_kernel(const ToppArgs a) {
 }
 
 // ------------------------------------------------- grid sizing (host)
-
-// Resident CTAs of a kernel on the current device, cached per device.
-template <typename K>
-int resident_ctas(K kernel, int slot) {
-    constexpr int kMaxDev = 64;
-    static std::atomic<int> cache[kMaxDev][4];
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
-    int v = cache[dev][slot].load(std::memory_order_relaxed);
-    if (v > 0) return v;
-    int sms = 0, per_sm = 0;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0) !=
-            cudaSuccess)
-        return 0;
-    v = sms * (per_sm > 0 ? per_sm : 1);
-    cache[dev][slot].store(v, std::memory_order_relaxed);
-    return v;
-}
 
 template <typename T, int KIND>
 int launch_stream_t(const RowView &rows, const SeqArgs &seq, int rows_total, float c,
