@@ -44,7 +44,7 @@ FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 7900.0
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "stream_kernel_c3.md")
 KERNEL_SOURCES = [os.path.join(ROOT, "speculative_decoding_verification_top_gb300", "csrc", f)
-                  for f in ("common.cuh", "rows.cu")]
+                  for f in ("common.cuh", "stream.cuh", "rows.cu")]
 
 
 def parse():
@@ -244,38 +244,45 @@ class Job:
         else:
             sv.spec_verify_sample(*self.chain_args(i))
 
-    def phases(self, i, ev_mid_a, ev_mid_b):
-        """One chain step as its two phases, events around the row kernel."""
-        args = self.chain_args(i)
-        ev_mid_a.record(self.stream)
-        self.sv.spec_verify_sample_rows(*args)
-        ev_mid_b.record(self.stream)
-        self.sv.spec_verify_sample_finish(*args)
+    def rows_only(self, i, ev_a, ev_b):
+        """The row kernel of one chain step alone, between two events."""
+        ev_a.record(self.stream)
+        self.sv.spec_verify_sample_rows(*self.chain_args(i))
+        ev_b.record(self.stream)
 
 
-def timed_device(job, steps, warmup, world):
+def timed_device(job, steps, warmup, world, kernel_launches=500):
+    """Whole verify calls back to back (nothing enqueued between them), then,
+    for the roofline, the row kernel alone in launches bracketed by events."""
     import torch
     for i in range(warmup):
         job.step(i)
     torch.cuda.synchronize()
-    chain = job.mode != "tree"
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
-    mids = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in range(steps)] if chain else []
     barrier(world)
     torch.cuda.synchronize()
     ev0.record(job.stream)
     for i in range(steps):
-        if chain:
-            job.phases(i, *mids[i])
-        else:
-            job.step(i)
+        job.step(i)
     ev1.record(job.stream)
     torch.cuda.synchronize()
     barrier(world)
     total_ms = ev0.elapsed_time(ev1)
-    rows_ms = float(np.mean([a.elapsed_time(b) for a, b in mids])) if chain else None
+    rows_ms = None
+    if job.mode != "tree":
+        n = min(steps, kernel_launches)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n)]
+        for i in range(3):
+            job.rows_only(i, *evs[0])
+        torch.cuda.synchronize()
+        for i, (a, b) in enumerate(evs):
+            job.rows_only(i, a, b)
+        torch.cuda.synchronize()
+        rows_ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
+        job.step(0)  # leave the workspace as a finished call left it
+        torch.cuda.synchronize()
     return total_ms, rows_ms
 
 

@@ -25,8 +25,9 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 _ROOT = os.path.dirname(_PKG)
 LIB_PATH = os.path.join(_PKG, "libspecverify.so")
 CSRC = os.path.join(_PKG, "csrc")
-SOURCES = [os.path.join(CSRC, f) for f in ("api.cu", "rows.cu", "final.cu", "noalloc.cu")]
-HEADERS = [os.path.join(CSRC, "common.cuh")]
+SOURCES = [os.path.join(CSRC, f)
+           for f in ("api.cu", "rows.cu", "final.cu", "noalloc.cu")]
+HEADERS = [os.path.join(CSRC, f) for f in ("common.cuh", "stream.cuh", "draw.cuh")]
 INCLUDE = os.path.join(_ROOT, "include")
 HEADER = os.path.join(INCLUDE, "spec_verify.h")
 BUILD_DIR = os.path.join(_PKG, "_build")

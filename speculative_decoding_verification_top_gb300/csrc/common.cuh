@@ -57,7 +57,7 @@ struct SeqRec {         // one sequence's accept decision (and debug values)
     float pneg, pinv;  // -(m c) and 1/z of the draw's target row
     float qneg, qinv;  // the same for the draft row (residual only)
     uint32_t plam, qlam;  // nucleus keys of the two rows
-    float pad[2];
+    uint32_t pad[2];
     float P[32];       // p_i(x~_i)
     float Q[32];       // q_i(x~_i)
 };
@@ -446,7 +446,7 @@ struct FinalArgs {
     const float *uniforms;
     int B, k, V;
     int NS;            // 1024-element sub-tiles per row
-    long long per;     // sub-tiles per warp (contiguous run in (b, t) order)
+    long long per;     // warps in the final kernel's grid (each takes an even share)
     float c;
     int32_t *out_tokens;
     int32_t *out_num;

@@ -267,8 +267,10 @@ def test_repeated_calls_are_bitwise_reproducible():
         np.testing.assert_array_equal(a, b)
 
 
-def test_two_phase_api_equals_single_call():
-    wl = workloads.c4(B=4)
+@pytest.mark.parametrize("make", [lambda: workloads.c4(B=4), lambda: workloads.c3(B=6)],
+                         ids=["top_p_rows", "stream_rows"])
+def test_two_phase_api_equals_single_call(make):
+    wl = make()
     t1, n1, _ = run_gpu(wl)
     tg, dr, tk, un = dev(wl.target), dev(wl.draft), dev(wl.draft_tokens), dev(wl.uniforms)
     out_t = torch.empty((wl.B, wl.k + 1), dtype=torch.int32, device=DEV)
