@@ -26,7 +26,7 @@ _ROOT = os.path.dirname(_PKG)
 LIB_PATH = os.path.join(_PKG, "libspecverify.so")
 CSRC = os.path.join(_PKG, "csrc")
 SOURCES = [os.path.join(CSRC, f)
-           for f in ("api.cu", "rows.cu", "final.cu", "noalloc.cu")]
+           for f in ("api.cu", "rows.cu", "topp.cu", "final.cu", "noalloc.cu")]
 HEADERS = [os.path.join(CSRC, f) for f in ("common.cuh", "stream.cuh", "draw.cuh")]
 INCLUDE = os.path.join(_ROOT, "include")
 HEADER = os.path.join(INCLUDE, "spec_verify.h")

@@ -11,11 +11,9 @@ namespace {
 constexpr size_t kAlign = 256;
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
-int tiles_for(int V) { return (V + kTileMax - 1) / kTileMax; }
-int tile_len(int V, int T) { return ((V + T - 1) / T + 7) / 8 * 8; }
 int subs_for(int V) { return (V + kSubW - 1) / kSubW; }
 // Partial slots per row: a row of V elements meets at most ceil(V / seg) + 1
-// warp segments (seg >= kMinSeg), and at most tiles_for(V) CTA tiles.
+// warp segments (seg >= kMinSeg).
 int pmax_for(int V) { return (V + kMinSeg - 1) / kMinSeg + 2; }
 
 // Carve the workspace; returns the bytes needed (base may be null).
@@ -55,12 +53,12 @@ bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 bool chain_sizes_ok(int B, int k, int V) {
     if (B < 0 || k < 1 || k > SPEC_MAX_K || V < 1 || V > SPEC_MAX_V) return false;
     const long long rows = static_cast<long long>(B) * (2 * k + 1);
-    return rows * tiles_for(V) < INT_MAX && static_cast<long long>(B) * subs_for(V) * 32 < INT_MAX;
+    return rows * pmax_for(V) < INT_MAX && static_cast<long long>(B) * subs_for(V) * 32 < INT_MAX;
 }
 
 bool tree_sizes_ok(int B, int N, int V) {
     if (B < 0 || N < 1 || N > SPEC_MAX_TREE_NODES || V < 1 || V > SPEC_MAX_V) return false;
-    return static_cast<long long>(B) * N * tiles_for(V) < INT_MAX;
+    return static_cast<long long>(B) * N * pmax_for(V) < INT_MAX;
 }
 
 struct ChainPlan {
@@ -137,21 +135,25 @@ int plan_chain(const void *target_logits, const void *draft_logits, const int32_
     return SPEC_OK;
 }
 
+// Row statistics and accept decisions.  With top-p the row kernel writes
+// the statistics only, and the top-p kernel selects each nucleus and
+// takes the decisions.
 int launch_chain_rows(const ChainPlan &p) {
-    if (p.use_topp) {
-        ToppArgs ta;
-        ta.rows = p.rows;
-        ta.seq = p.seq;
-        ta.T = tiles_for(p.rows.V);
-        ta.TL = tile_len(p.rows.V, ta.T);
-        ta.c = p.c;
-        ta.temperature = p.temperature;
-        ta.top_p = p.top_p;
-        ta.ws = p.ws;
-        return launch_topp_rows(ta, p.rows_total, p.dtype, p.st);
-    }
-    return launch_stream_rows(p.rows, p.seq, p.rows_total, p.c, p.ws, p.stoch ? 0 : 1, p.dtype,
-                              p.st);
+    if (!p.use_topp)
+        return launch_stream_rows(p.rows, p.seq, p.rows_total, p.c, p.ws, p.stoch ? 0 : 1,
+                                  p.dtype, p.st);
+    SeqArgs none = p.seq;
+    none.work = kSeqNone;
+    const int rc = launch_stream_rows(p.rows, none, p.rows_total, p.c, p.ws, 0, p.dtype, p.st);
+    if (rc != SPEC_OK) return rc;
+    ToppArgs ta;
+    ta.rows = p.rows;
+    ta.seq = p.seq;
+    ta.c = p.c;
+    ta.temperature = p.temperature;
+    ta.top_p = p.top_p;
+    ta.ws = p.ws;
+    return launch_topp_rows(ta, p.rows_total, p.dtype, p.st);
 }
 
 // Greedy verification completes inside the row kernel: nothing to finish.

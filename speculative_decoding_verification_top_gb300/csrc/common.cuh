@@ -20,9 +20,10 @@ constexpr int kThreads = 256;            // CTA size of the row and draw kernels
 constexpr int kWarps = kThreads / 32;
 constexpr int kBatch = 4;                // 16-byte vectors in flight per lane
 constexpr int kMinSeg = 2048;            // smallest warp segment (elements)
-constexpr int kTileMax = 16384;          // elements per CTA tile (top-p kernel)
 constexpr int kSubW = 1024;              // elements per draw sub-tile (a warp)
-constexpr int kHistBins = 2048;          // top-p radix bins per pass
+constexpr int kHistBins = 2048;          // top-p radix bins per pass (one CTA)
+constexpr int kElemCap = 1024;           // top-p select: logits of one histogram bin held in shared memory
+constexpr float kToppTry = 9.0f;         // top-p select: first try logits within 9 T of the max
 constexpr float kFix = 1099511627776.0f; // 2^40: fixed-point mass unit
 constexpr float kNegInf = -INFINITY;
 
@@ -195,6 +196,20 @@ __device__ __forceinline__ float batch_max<uint16_t>(const uint4 (&q)[kBatch]) {
     for (int u = 0; u < kBatch; ++u)
         m = max_nan_bf16x2(m, max_nan_bf16x2(max_nan_bf16x2(q[u].x, q[u].y),
                                              max_nan_bf16x2(q[u].z, q[u].w)));
+    return max_nan(__uint_as_float(m << 16), __uint_as_float(m & 0xFFFF0000u));
+}
+
+// NaN-propagating max of one vector.
+template <typename T>
+__device__ __forceinline__ float batch_max1(const uint4 &q);
+template <>
+__device__ __forceinline__ float batch_max1<float>(const uint4 &q) {
+    return max_nan(max_nan(__uint_as_float(q.x), __uint_as_float(q.y)),
+                   max_nan(__uint_as_float(q.z), __uint_as_float(q.w)));
+}
+template <>
+__device__ __forceinline__ float batch_max1<uint16_t>(const uint4 &q) {
+    const uint32_t m = max_nan_bf16x2(max_nan_bf16x2(q.x, q.y), max_nan_bf16x2(q.z, q.w));
     return max_nan(__uint_as_float(m << 16), __uint_as_float(m & 0xFFFF0000u));
 }
 
@@ -434,7 +449,6 @@ struct StreamArgs {
 struct ToppArgs {
     RowView rows;
     SeqArgs seq;
-    int T, TL;         // tiles per row, tile length
     float c, temperature, top_p;
     Workspace ws;
 };
@@ -485,10 +499,13 @@ int resident_ctas(K kernel, int slot) {
     return v;
 }
 
-// kind 0: stochastic statistics; kind 1: argmax.  dtype: SPEC_F32/SPEC_BF16.
-// Each returns SPEC_OK or SPEC_ERR_CUDA.
+// kind 0: stochastic statistics; kind 1: argmax.  dtype: SPEC_F32 /
+// SPEC_BF16.  Each returns SPEC_OK or SPEC_ERR_CUDA.
 int launch_stream_rows(const RowView &rows, const SeqArgs &seq, int rows_total, float c,
                        const Workspace &ws, int kind, int dtype, cudaStream_t st);
+// The top-p select (one CTA per row) runs after the row kernel (kind 0,
+// no sequence work) and takes the accept decisions; launched as its
+// programmatic dependent.
 int launch_topp_rows(const ToppArgs &a, int rows_total, int dtype, cudaStream_t st);
 // The final kernel is launched as a programmatic dependent of the row kernel.
 int launch_final(const FinalArgs &a, int dtype, cudaStream_t st);

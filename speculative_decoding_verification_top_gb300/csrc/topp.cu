@@ -1,0 +1,361 @@
+// topp.cu -- the top-p (nucleus) threshold of every row, and the accept
+// decisions that depend on it.
+//
+// "3.5 Speculative Decoding" (llm-learning-path), "Notation": p and q are
+// the target and draft distributions after temperature and top-p; the
+// pages name the nucleus but never define it.  Reading: keep the most
+// likely tokens until their mass reaches top_p, all ties of the last one
+// kept; the kept set is {x : key(l_x) >= lam}, lam the largest key whose
+// mass from the top reaches top_p Z.  Masses are fixed-point integers
+// (2^-40 units) so every histogram sum is exact and order-independent.
+//
+// topp_kernel  one CTA per row, after the row kernel has written the row's
+//              max m and normaliser Z.
+//   1. Tokens below c0 = m + T (ln((1 - top_p) Z / V) - ln 2) cannot be in
+//      the nucleus: all of them together carry < V e(c0) <= (1 - top_p) Z / 2.
+//   2. Pass A reads the row and histograms the mass of its logits >= y by
+//      value, uniformly over [y, m] (bins of keys would crowd the bulk of a
+//      row into a few bins: keys are log-spaced).  It first tries y = m -
+//      kToppTry T (a nucleus usually ends far above c0, and the logits in
+//      between are most of the work); if the mass of the logits >= y falls
+//      short of top_p Z it runs again with y = c0.  The bin where the mass
+//      from the top first reaches top_p Z holds lam.
+//      Pass A also keeps the logits it histogrammed in shared memory when
+//      they fit (kAList; a few percent of a peaked row).
+//   3. Pass B gathers the logits of that bin -- the same float arithmetic
+//      decides membership in both passes -- from that list (or, if it
+//      overflowed, from a second read of the row, which skips a 16-byte
+//      vector whose max is below the bin) and histograms them by key,
+//      narrowing until one key is left: the largest key whose mass from the
+//      top reaches top_p Z.  (A bin holding more than kElemCap logits is
+//      narrowed from the row.)
+//   The row record gets lam and the kept mass; the warp that finishes a
+//   sequence's last row takes its accept decision.
+
+#include "common.cuh"
+
+namespace specv {
+namespace {
+
+constexpr int kTpThreads = 128;  // one CTA per row; small, so that a whole batch fits one wave
+constexpr int kTpWarps = kTpThreads / 32;
+constexpr int kAList = 3072;     // logits kept from pass A (shared memory)
+
+struct SelShared {
+    unsigned long long hist[kHistBins];
+    unsigned long long wsum[kTpWarps];
+    unsigned long long b_above, hb;
+    int cross, lastnz;
+};
+
+// Block-wide scan of the histogram and the crossing bin: the first bin
+// (from the top) where above + the mass so far reaches tgt, else the last
+// bin holding mass (or 0).  Returns the bin; *b_above gets the mass of the
+// bins before it, *hb the bin's own mass, *crossed whether it crossed.
+__device__ int cta_cross(SelShared &sh, int nb, unsigned long long above, unsigned long long tgt,
+                         unsigned long long *b_above, unsigned long long *hb, bool *crossed) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int kPer = kHistBins / kTpThreads;
+    unsigned long long h[kPer], mine = 0ull;
+    int lastnz = -1;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+        h[i] = sh.hist[tid * kPer + i];
+        mine += h[i];
+        if (h[i]) lastnz = tid * kPer + i;
+    }
+    unsigned long long x = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) sh.wsum[warp] = x;
+    __syncthreads();
+    unsigned long long before = above + x - mine;
+    for (int i = 0; i < warp; ++i) before += sh.wsum[i];
+    {
+        unsigned long long run = before;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            run += h[i];
+            if (run >= tgt && tid * kPer + i < nb) {
+                atomicMin(&sh.cross, tid * kPer + i);
+                break;
+            }
+        }
+    }
+    if (lastnz >= 0) atomicMax(&sh.lastnz, lastnz);
+    __syncthreads();
+    *crossed = sh.cross != INT_MAX;
+    const int b = *crossed ? sh.cross : max(sh.lastnz, 0);
+    if (tid == b / kPer) {
+        unsigned long long run = before;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i)
+            if (tid * kPer + i < b) run += h[i];
+        sh.b_above = run;
+        sh.hb = h[b - tid * kPer];
+    }
+    __syncthreads();
+    *b_above = sh.b_above;
+    *hb = sh.hb;
+    __syncthreads();  // every thread has read sh before it is reset
+    return b;
+}
+
+__device__ __forceinline__ void cta_clear(SelShared &sh) {
+    for (int i = threadIdx.x; i < kHistBins; i += kTpThreads) sh.hist[i] = 0ull;
+    if (threadIdx.x == 0) {
+        sh.cross = INT_MAX;
+        sh.lastnz = -1;
+    }
+    __syncthreads();
+}
+
+struct ToppShared {
+    SelShared sel;
+    float alist[kAList];            // the logits pass A histogrammed (when they fit)
+    float elems[kElemCap];          // the logits of the crossing bin (pass B from global)
+    float queue[kTpWarps][32 * 8];  // one vector slot of one warp (32 lanes x 8 logits)
+    int n_alist, n_elems;
+    unsigned int kmin, kmax;
+};
+
+// Every logit >= vmin of a row from global memory, calling `f(l)` on each.
+// Warp w streams the w-th quarter of the row's 16-byte vectors (kBatch per
+// lane in flight, the next batch loaded while this one is reduced).  For
+// every vector slot of a batch the warp first packs its logits >= vmin into
+// its shared queue, all lanes converged, then calls f on the queue densely:
+// those logits are sparse, and calling f where they lie would run f's path
+// once per element slot for nearly every slot.
+template <typename T, typename F>
+__device__ __forceinline__ void for_row(ToppShared &sh, const T *rowp, int V, float vmin, F &&f) {
+    constexpr int P = Elem<T>::kPerVec;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    float *q_w = sh.queue[warp];
+    const Span<T> sp(rowp, 0, V);
+    if (tid < sp.a0 - sp.e0) {
+        const float l = to_f32(rowp[sp.e0 + tid]);
+        if (l >= vmin) f(l);
+    }
+    if (tid < sp.e1 - sp.a1) {
+        const float l = to_f32(rowp[sp.a1 + tid]);
+        if (l >= vmin) f(l);
+    }
+    const int per = (sp.nvec + kTpWarps - 1) / kTpWarps;
+    const int v0w = min(sp.nvec, warp * per), n = min(sp.nvec, v0w + per) - v0w;
+    const uint4 *vp = reinterpret_cast<const uint4 *>(rowp + sp.a0) + v0w;
+    const uint4 neg = neg_inf_vec<T>();
+    constexpr int kStride = 32 * kBatch;
+    uint4 q[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) q[u] = lane + u * 32 < n ? ld_stream(vp + lane + u * 32) : neg;
+    for (int b0 = 0; b0 < n; b0 += kStride) {  // warp-uniform trip count
+        uint4 nq[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int v = b0 + kStride + u * 32 + lane;
+            nq[u] = v < n ? ld_stream(vp + v) : neg;
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            float h[P];
+            unpack<T>(q[u], h);
+            uint32_t mask = 0u;
+            if (batch_max1<T>(q[u]) >= vmin) {
+#pragma unroll
+                for (int e = 0; e < P; ++e)
+                    if (h[e] >= vmin) mask |= 1u << e;
+            }
+            const unsigned any = __ballot_sync(0xFFFFFFFFu, mask != 0u);
+            if (!any) continue;
+            const int cnt = __popc(mask);
+            int incl = cnt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            const int tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+            int pos = incl - cnt;
+#pragma unroll
+            for (int e = 0; e < P; ++e)
+                if (mask & (1u << e)) q_w[pos++] = h[e];
+            __syncwarp();
+            for (int i = lane; i < tot; i += 32) f(q_w[i]);
+            __syncwarp();
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) q[u] = nq[u];
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kTpThreads, 6) topp_kernel(const ToppArgs a) {
+    // The row kernel's records must be complete and visible; then let the
+    // final kernel launch.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    extern __shared__ __align__(16) unsigned char topp_smem[];
+    ToppShared &sh = *reinterpret_cast<ToppShared *>(topp_smem);
+    const int row = blockIdx.x, tid = threadIdx.x;
+    RowRec *rec = a.ws.rows + row;
+    const float m = __ldcg(&rec->m);
+    const float Z = __ldcg(&rec->z_full);
+    const uint32_t flags = __ldcg(&rec->flags);
+    uint32_t lam = 0u;
+    float zk = Z;
+    if (flags == 0u) {
+        const int V = a.rows.V;
+        const float c = a.c;
+        const float negmc = -__fmul_rn(m, c);
+        const unsigned long long tgt =
+            __float2ull_rn(__fmul_rn(__fmul_rn(a.top_p, Z), kFix));
+        const float c0 = m + a.temperature *
+                                 (logf((1.0f - a.top_p) * Z / static_cast<float>(V)) - 0.69314718f);
+        const float cut = fminf(c0, m);
+        const T *rowp = row_ptr<T>(a.rows, row);
+        // Pass A first over [y1, m]: y1 = m - kToppTry T, or c0 if higher.
+        // If the mass of the logits >= y1 already reaches top_p Z the
+        // crossing bin is found there (exactly: the histogram holds every
+        // logit >= y1); otherwise pass A runs again over [c0, m].
+        float lo = fmaxf(cut, m - kToppTry * a.temperature);
+        float span = 0.0f, inv = 0.0f;
+        auto vbin = [&](float l) {
+            return min(static_cast<int>(__fmul_rn(__fsub_rn(m, l), inv)), kHistBins - 1);
+        };
+        auto mass = [&](float l) {
+            return __float2ull_rn(__fmul_rn(ex2(__fmaf_rn(l, c, negmc)), kFix));
+        };
+        unsigned long long above = 0ull, hb = 0ull;
+        int b0 = 0;
+        for (int attempt = 0; attempt < 2; ++attempt) {
+            span = __fsub_rn(m, lo);
+            inv = span > 0.0f ? static_cast<float>(kHistBins) / span : 0.0f;
+            cta_clear(sh.sel);
+            if (tid == 0) sh.n_alist = 0;
+            __syncthreads();
+            for_row<T>(sh, rowp, V, lo, [&](float l) {
+                atomicAdd(&sh.sel.hist[vbin(l)], mass(l));
+                const int pos = atomicAdd(&sh.n_alist, 1);
+                if (pos < kAList) sh.alist[pos] = l;
+            });
+            __syncthreads();
+            bool crossed;
+            b0 = cta_cross(sh.sel, kHistBins, 0ull, tgt, &above, &hb, &crossed);
+            if (crossed || lo == cut) break;
+            lo = cut;
+        }
+        // Pass B: the logits of bin b0 and their key range.  No logit below
+        // vmin can fall into b0 (the margin exceeds any rounding of vbin).
+        const float vlo =
+            b0 == kHistBins - 1
+                ? lo
+                : __fsub_rn(m, __fmul_rn(static_cast<float>(b0 + 1), span / kHistBins));
+        const float vmin =
+            fmaxf(lo, vlo - span * 9.5367431640625e-7f - fabsf(vlo) * 9.5367431640625e-7f);
+        if (tid == 0) {
+            sh.n_elems = 0;
+            sh.kmin = 0xFFFFFFFFu;
+            sh.kmax = 0u;
+        }
+        __syncthreads();
+        const int na = sh.n_alist;
+        auto take = [&](float l) {
+            if (l >= lo && vbin(l) == b0) {
+                const int pos = atomicAdd(&sh.n_elems, 1);
+                if (pos < kElemCap) sh.elems[pos] = l;
+                atomicMin(&sh.kmin, okey<T>(l));
+                atomicMax(&sh.kmax, okey<T>(l));
+            }
+        };
+        if (na <= kAList) {
+            for (int i = tid; i < na; i += kTpThreads) take(sh.alist[i]);
+        } else {
+            for_row<T>(sh, rowp, V, vmin, take);
+        }
+        __syncthreads();
+        const int ne = sh.n_elems;
+        uint32_t klo = sh.kmin, khi = sh.kmax;
+        // Narrow by key inside bin b0.
+        for (int pass = 0; pass < 4 && khi > klo; ++pass) {
+            const unsigned long long W = static_cast<unsigned long long>(khi - klo) + 1ull;
+            const int nb = W < static_cast<unsigned long long>(kHistBins) ? static_cast<int>(W)
+                                                                           : kHistBins;
+            cta_clear(sh.sel);
+            auto add = [&](float l) {
+                const uint32_t key = okey<T>(l);
+                if (key < klo || key > khi) return;
+                const int bin =
+                    static_cast<int>((static_cast<unsigned long long>(khi - key) * nb) / W);
+                atomicAdd(&sh.sel.hist[bin], mass(l));
+            };
+            if (ne <= kElemCap) {
+                for (int i = tid; i < ne; i += kTpThreads) add(sh.elems[i]);
+            } else {
+                for_row<T>(sh, rowp, V, vmin, [&](float l) {
+                    if (l >= lo && vbin(l) == b0) add(l);
+                });
+            }
+            __syncthreads();
+            bool cr;
+            unsigned long long ab;
+            const int b = cta_cross(sh.sel, nb, above, tgt, &ab, &hb, &cr);
+            above = ab;
+            const unsigned long long lo_off = (static_cast<unsigned long long>(b) * W + nb - 1) / nb;
+            const unsigned long long hi_off =
+                (static_cast<unsigned long long>(b + 1) * W + nb - 1) / nb - 1;
+            const uint32_t nkhi = khi - static_cast<uint32_t>(lo_off);
+            klo = khi - static_cast<uint32_t>(hi_off);
+            khi = nkhi;
+        }
+        lam = khi;
+        zk = __fmul_rn(__ull2float_rn(khi == klo ? above + hb : tgt), 1.0f / kFix);
+    }
+    if (tid == 0) {
+        rec->z = zk;
+        rec->lam_key = lam;
+    }
+    __syncthreads();
+    if (tid < 32) row_done<T>(a.rows, a.seq, a.ws, a.c, row);
+}
+
+// Opt each instantiation into ToppShared's dynamic shared memory, once per
+// device.
+template <typename K>
+bool topp_smem_ok(K kernel, int slot) {
+    constexpr int kMaxDev = 64;
+    static int done[kMaxDev][2];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return false;
+    if (__atomic_load_n(&done[dev][slot], __ATOMIC_RELAXED)) return true;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(sizeof(ToppShared))) != cudaSuccess)
+        return false;
+    __atomic_store_n(&done[dev][slot], 1, __ATOMIC_RELAXED);
+    return true;
+}
+
+}  // namespace
+
+int launch_topp_rows(const ToppArgs &a, int rows_total, int dtype, cudaStream_t st) {
+    const bool ok = dtype == SPEC_F32 ? topp_smem_ok(topp_kernel<float>, 0)
+                                      : topp_smem_ok(topp_kernel<uint16_t>, 1);
+    if (!ok) return SPEC_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(rows_total));
+    cfg.blockDim = dim3(kTpThreads);
+    cfg.dynamicSmemBytes = sizeof(ToppShared);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = dtype == SPEC_F32 ? cudaLaunchKernelEx(&cfg, topp_kernel<float>, a)
+                                            : cudaLaunchKernelEx(&cfg, topp_kernel<uint16_t>, a);
+    return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+}  // namespace specv
