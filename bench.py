@@ -385,10 +385,14 @@ def run_ours(args):
     e2e_value = world * nbytes * args.e2e_steps / (e2e_ms * 1e-3) / 1e9
 
     if rows_ms is not None:
+        # The row phase: one stream_kernel launch, or with top-p the
+        # stream_kernel and topp_kernel pair (timed together).
+        topp = wl.top_p < 1.0
         achieved = nbytes / (rows_ms * 1e-3) / 1e9
-        roofline = {"bound": "hbm", "kernel": "stream_kernel", "achieved": round(achieved, 1),
+        roofline = {"bound": "hbm", "kernel": "stream_kernel+topp_kernel" if topp else "stream_kernel",
+                    "achieved": round(achieved, 1),
                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                    "frac": round(achieved / peak, 4), "traffic": profiled_traffic(),
+                    "frac": round(achieved / peak, 4), "traffic": None if topp else profiled_traffic(),
                     "algorithmic_bytes": nbytes, "avg_launch_us": round(rows_ms * 1e3, 2)}
     else:
         per_launch_ms = ms_step  # the tree call: argmax rows kernel dominates
