@@ -135,17 +135,12 @@ int plan_chain(const void *target_logits, const void *draft_logits, const int32_
     return SPEC_OK;
 }
 
-// Row statistics and accept decisions.  With top-p the row kernel writes
-// the statistics only, and the top-p kernel selects each nucleus and
-// takes the decisions.
+// Row statistics and accept decisions.  With top-p one kernel does both
+// for every row (statistics, then the nucleus), and takes the decisions.
 int launch_chain_rows(const ChainPlan &p) {
     if (!p.use_topp)
         return launch_stream_rows(p.rows, p.seq, p.rows_total, p.c, p.ws, p.stoch ? 0 : 1,
                                   p.dtype, p.st);
-    SeqArgs none = p.seq;
-    none.work = kSeqNone;
-    const int rc = launch_stream_rows(p.rows, none, p.rows_total, p.c, p.ws, 0, p.dtype, p.st);
-    if (rc != SPEC_OK) return rc;
     ToppArgs ta;
     ta.rows = p.rows;
     ta.seq = p.seq;

@@ -503,9 +503,8 @@ int resident_ctas(K kernel, int slot) {
 // SPEC_BF16.  Each returns SPEC_OK or SPEC_ERR_CUDA.
 int launch_stream_rows(const RowView &rows, const SeqArgs &seq, int rows_total, float c,
                        const Workspace &ws, int kind, int dtype, cudaStream_t st);
-// The top-p select (one CTA per row) runs after the row kernel (kind 0,
-// no sequence work) and takes the accept decisions; launched as its
-// programmatic dependent.
+// With top-p one CTA per row reduces the row's statistics, selects its
+// nucleus and takes the accept decisions (instead of the row kernel).
 int launch_topp_rows(const ToppArgs &a, int rows_total, int dtype, cudaStream_t st);
 // The final kernel is launched as a programmatic dependent of the row kernel.
 int launch_final(const FinalArgs &a, int dtype, cudaStream_t st);

@@ -9,8 +9,8 @@
 // mass from the top reaches top_p Z.  Masses are fixed-point integers
 // (2^-40 units) so every histogram sum is exact and order-independent.
 //
-// topp_kernel  one CTA per row, after the row kernel has written the row's
-//              max m and normaliser Z.
+// topp_kernel  one CTA per row.  It first reduces the row's max m and
+//              normaliser Z itself (8 warps, a split fixed by V), then:
 //   1. Tokens below c0 = m + T (ln((1 - top_p) Z / V) - ln 2) cannot be in
 //      the nucleus: all of them together carry < V e(c0) <= (1 - top_p) Z / 2.
 //   2. Pass A reads the row and histograms the mass of its logits >= y by
@@ -32,14 +32,20 @@
 //   The row record gets lam and the kept mass; the warp that finishes a
 //   sequence's last row takes its accept decision.
 
-#include "common.cuh"
+#include "stream.cuh"
 
 namespace specv {
 namespace {
 
-constexpr int kTpThreads = 128;  // one CTA per row; small, so that a whole batch fits one wave
+constexpr int kTpThreads = 256;  // one CTA per row
 constexpr int kTpWarps = kTpThreads / 32;
 constexpr int kAList = 3072;     // logits kept from pass A (shared memory)
+// Shared memory requested per CTA: more than the select needs, so that at
+// most three CTAs share an SM and the rows being selected (3 x 152 rows of
+// ~256 KB for bf16 V=128k) mostly stay in the 126 MB L2 between a CTA's
+// two reads of its row.  (Measured on c4: 2 per SM leaves HBM idle while
+// both CTAs of an SM select; 4 per SM spills registers and overflows L2.)
+constexpr int kToppSmem = 72 * 1024;
 
 struct SelShared {
     unsigned long long hist[kHistBins];
@@ -113,17 +119,23 @@ __device__ __forceinline__ void cta_clear(SelShared &sh) {
     __syncthreads();
 }
 
+struct ToppShared;
 struct ToppShared {
     SelShared sel;
     float alist[kAList];            // the logits pass A histogrammed (when they fit)
     float elems[kElemCap];          // the logits of the crossing bin (pass B from global)
     float queue[kTpWarps][32 * 8];  // one vector slot of one warp (32 lanes x 8 logits)
+    float pm[kTpWarps], ps[kTpWarps];
+    uint32_t pf[kTpWarps];
+    float m, Z;
+    uint32_t flags;
     int n_alist, n_elems;
     unsigned int kmin, kmax;
 };
+static_assert(sizeof(ToppShared) <= kToppSmem, "top-p shared memory");
 
 // Every logit >= vmin of a row from global memory, calling `f(l)` on each.
-// Warp w streams the w-th quarter of the row's 16-byte vectors (kBatch per
+// Warp w streams the w-th eighth of the row's 16-byte vectors (kBatch per
 // lane in flight, the next batch loaded while this one is reduced).  For
 // every vector slot of a batch the warp first packs its logits >= vmin into
 // its shared queue, all lanes converged, then calls f on the queue densely:
@@ -192,30 +204,59 @@ __device__ __forceinline__ void for_row(ToppShared &sh, const T *rowp, int V, fl
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kTpThreads, 6) topp_kernel(const ToppArgs a) {
-    // The row kernel's records must be complete and visible; then let the
-    // final kernel launch.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+__global__ void __launch_bounds__(kTpThreads, 3) topp_kernel(const ToppArgs a) {
+    // Let the dependent final-draw grid launch once every CTA of this grid
+    // has started (it waits for this grid's completion before reading).
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     extern __shared__ __align__(16) unsigned char topp_smem[];
     ToppShared &sh = *reinterpret_cast<ToppShared *>(topp_smem);
     const int row = blockIdx.x, tid = threadIdx.x;
     RowRec *rec = a.ws.rows + row;
-    const float m = __ldcg(&rec->m);
-    const float Z = __ldcg(&rec->z_full);
-    const uint32_t flags = __ldcg(&rec->flags);
+    const T *rowp = row_ptr<T>(a.rows, row);
+    {
+        // Row statistics: warp w reduces the w-th eighth of the row (a
+        // split fixed by V alone), combined in warp order.
+        const int V = a.rows.V, warp = tid >> 5;
+        const int per = ((V + kTpWarps - 1) / kTpWarps + 7) / 8 * 8;
+        const int lo = min(V, warp * per), hi = min(V, lo + per);
+        float pm = kNegInf, ps = 0.0f;
+        uint32_t pf = 0u;
+        warp_piece_ms<T>(rowp, lo, hi, a.c, pm, ps, pf);
+        warp_reduce_ms(pm, ps, pf, a.c);
+        if ((tid & 31) == 0) {
+            sh.pm[warp] = pm;
+            sh.ps[warp] = ps;
+            sh.pf[warp] = pf;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            float mm = sh.pm[0], ss = sh.ps[0];
+            uint32_t ff = sh.pf[0];
+            for (int w = 1; w < kTpWarps; ++w) {
+                ms_combine(mm, ss, sh.pm[w], sh.ps[w], a.c);
+                ff |= sh.pf[w];
+            }
+            sh.m = mm;
+            sh.Z = ss;
+            sh.flags = row_flags(mm, ff);
+        }
+        __syncthreads();
+    }
+    const float m = sh.m;
+    const float Z = sh.Z;
+    const uint32_t flags = sh.flags;
     uint32_t lam = 0u;
     float zk = Z;
     if (flags == 0u) {
         const int V = a.rows.V;
         const float c = a.c;
         const float negmc = -__fmul_rn(m, c);
+        __syncthreads();
         const unsigned long long tgt =
             __float2ull_rn(__fmul_rn(__fmul_rn(a.top_p, Z), kFix));
         const float c0 = m + a.temperature *
                                  (logf((1.0f - a.top_p) * Z / static_cast<float>(V)) - 0.69314718f);
         const float cut = fminf(c0, m);
-        const T *rowp = row_ptr<T>(a.rows, row);
         // Pass A first over [y1, m]: y1 = m - kToppTry T, or c0 if higher.
         // If the mass of the logits >= y1 already reaches top_p Z the
         // crossing bin is found there (exactly: the histogram holds every
@@ -314,8 +355,15 @@ __global__ void __launch_bounds__(kTpThreads, 6) topp_kernel(const ToppArgs a) {
         zk = __fmul_rn(__ull2float_rn(khi == klo ? above + hb : tgt), 1.0f / kFix);
     }
     if (tid == 0) {
-        rec->z = zk;
-        rec->lam_key = lam;
+        RowRec r;
+        r.m = m;
+        r.z = zk;
+        r.lam_key = lam;
+        r.arg = 0;
+        r.z_full = Z;
+        r.flags = flags;
+        r.pad[0] = r.pad[1] = 0;
+        *rec = r;
     }
     __syncthreads();
     if (tid < 32) row_done<T>(a.rows, a.seq, a.ws, a.c, row);
@@ -331,7 +379,7 @@ bool topp_smem_ok(K kernel, int slot) {
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return false;
     if (__atomic_load_n(&done[dev][slot], __ATOMIC_RELAXED)) return true;
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(sizeof(ToppShared))) != cudaSuccess)
+                             kToppSmem) != cudaSuccess)
         return false;
     __atomic_store_n(&done[dev][slot], 1, __ATOMIC_RELAXED);
     return true;
@@ -346,13 +394,8 @@ int launch_topp_rows(const ToppArgs &a, int rows_total, int dtype, cudaStream_t 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(rows_total));
     cfg.blockDim = dim3(kTpThreads);
-    cfg.dynamicSmemBytes = sizeof(ToppShared);
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.dynamicSmemBytes = kToppSmem;
+    cfg.stream = st;  // first kernel of a call: plain stream order
     const cudaError_t e = dtype == SPEC_F32 ? cudaLaunchKernelEx(&cfg, topp_kernel<float>, a)
                                             : cudaLaunchKernelEx(&cfg, topp_kernel<uint16_t>, a);
     return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
