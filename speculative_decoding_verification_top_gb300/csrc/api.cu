@@ -17,7 +17,9 @@ int subs_for(int V) { return (V + kSubW - 1) / kSubW; }
 int pmax_for(int V) { return (V + kMinSeg - 1) / kMinSeg + 2; }
 
 // Carve the workspace; returns the bytes needed (base may be null).
-size_t carve(void *base, int B, int rows_per_seq, int V, Workspace *ws) {
+// `chain`: a chain call (rows_per_seq = 2k+1), which also needs the top-p
+// nucleus lists of its B (k+1) target rows; a tree call does not.
+size_t carve(void *base, int B, int rows_per_seq, int V, Workspace *ws, bool chain) {
     const size_t rows = static_cast<size_t>(B) * rows_per_seq;
     const int pmax = pmax_for(V), NS = subs_for(V);
     size_t off = 0;
@@ -34,6 +36,9 @@ size_t carve(void *base, int B, int rows_per_seq, int V, Workspace *ws) {
     char *rowrec = take(rows * sizeof(RowRec));
     char *subs = take(static_cast<size_t>(B) * NS * sizeof(float));
     char *seqs = take(static_cast<size_t>(B) * sizeof(SeqRec));
+    const size_t trows = chain ? static_cast<size_t>(B) * ((rows_per_seq + 1) / 2) : 0;
+    char *nuc_n = take(trows * sizeof(int32_t));
+    char *nuc = take(trows * kNucCap * sizeof(uint4));
     if (ws) {
         ws->err = reinterpret_cast<uint32_t *>(err);
         ws->row_ctr = reinterpret_cast<uint32_t *>(row_ctr);
@@ -43,6 +48,8 @@ size_t carve(void *base, int B, int rows_per_seq, int V, Workspace *ws) {
         ws->rows = reinterpret_cast<RowRec *>(rowrec);
         ws->sub_sums = reinterpret_cast<float *>(subs);
         ws->seqs = reinterpret_cast<SeqRec *>(seqs);
+        ws->nuc_n = reinterpret_cast<int32_t *>(nuc_n);
+        ws->nuc = reinterpret_cast<uint4 *>(nuc);
         ws->pmax = pmax;
     }
     return off;
@@ -91,7 +98,7 @@ int plan_chain(const void *target_logits, const void *draft_logits, const int32_
         !aligned(draft_tokens, 4) || (stoch && !aligned(uniforms, 4)) ||
         !aligned(out_tokens, 4) || !aligned(out_num_accepted, 4) || !aligned(workspace, 16))
         return SPEC_ERR_ALIGN;
-    if (workspace_bytes < carve(nullptr, B, 2 * k + 1, V, nullptr)) return SPEC_ERR_WORKSPACE;
+    if (workspace_bytes < carve(nullptr, B, 2 * k + 1, V, nullptr, true)) return SPEC_ERR_WORKSPACE;
 
     plan->stoch = stoch;
     plan->dtype = dtype;
@@ -100,7 +107,7 @@ int plan_chain(const void *target_logits, const void *draft_logits, const int32_
     plan->use_topp = stoch && top_p < 1.0f;
     plan->c = static_cast<float>(1.4426950408889634 / static_cast<double>(plan->temperature));
     plan->st = reinterpret_cast<cudaStream_t>(stream);
-    carve(workspace, B, 2 * k + 1, V, &plan->ws);
+    carve(workspace, B, 2 * k + 1, V, &plan->ws, true);
 
     RowView &rv = plan->rows;
     rv.target = target_logits;
@@ -128,6 +135,7 @@ int plan_chain(const void *target_logits, const void *draft_logits, const int32_
 
     SeqArgs &sq = plan->seq;
     sq.work = stoch ? kSeqDecide : kSeqGreedy;
+    sq.list_draw = stoch && top_p < 1.0f ? 1 : 0;
     sq.draft_tokens = draft_tokens;
     sq.uniforms = uniforms;
     sq.out_tokens = out_tokens;
@@ -164,14 +172,14 @@ using namespace specv;
 SPEC_EXPORT int spec_verify_workspace_size(int B, int k, int V, size_t *bytes) {
     if (!bytes) return SPEC_ERR_NULL;
     if (!chain_sizes_ok(B, k, V)) return SPEC_ERR_SHAPE;
-    *bytes = carve(nullptr, B, 2 * k + 1, V, nullptr);
+    *bytes = carve(nullptr, B, 2 * k + 1, V, nullptr, true);
     return SPEC_OK;
 }
 
 SPEC_EXPORT int spec_verify_tree_workspace_size(int B, int N, int V, size_t *bytes) {
     if (!bytes) return SPEC_ERR_NULL;
     if (!tree_sizes_ok(B, N, V)) return SPEC_ERR_SHAPE;
-    *bytes = carve(nullptr, B, N, V, nullptr);
+    *bytes = carve(nullptr, B, N, V, nullptr, false);
     return SPEC_OK;
 }
 
@@ -243,11 +251,11 @@ SPEC_EXPORT int spec_verify_tree(const void *target_logits, const int32_t *paren
         !aligned(out_tokens, 4) || !aligned(out_num_accepted, 4) ||
         (out_path && !aligned(out_path, 4)) || !aligned(workspace, 16))
         return SPEC_ERR_ALIGN;
-    if (workspace_bytes < carve(nullptr, B, N, V, nullptr)) return SPEC_ERR_WORKSPACE;
+    if (workspace_bytes < carve(nullptr, B, N, V, nullptr, false)) return SPEC_ERR_WORKSPACE;
 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     Workspace ws;
-    carve(workspace, B, N, V, &ws);
+    carve(workspace, B, N, V, &ws, false);
     RowView rv;
     rv.target = target_logits;
     rv.draft = nullptr;
@@ -292,10 +300,10 @@ SPEC_EXPORT int spec_verify_intermediates(const void *workspace, size_t workspac
                                           spec_stream_t stream) {
     if (!workspace) return SPEC_ERR_NULL;
     if (!chain_sizes_ok(B, k, V)) return SPEC_ERR_SHAPE;
-    if (workspace_bytes < carve(nullptr, B, 2 * k + 1, V, nullptr)) return SPEC_ERR_WORKSPACE;
+    if (workspace_bytes < carve(nullptr, B, 2 * k + 1, V, nullptr, true)) return SPEC_ERR_WORKSPACE;
     if (B == 0) return SPEC_OK;
     Workspace ws;
-    carve(const_cast<void *>(workspace), B, 2 * k + 1, V, &ws);
+    carve(const_cast<void *>(workspace), B, 2 * k + 1, V, &ws, true);
     return launch_intermediates(ws, B, k, P, Q, Z, S, reinterpret_cast<cudaStream_t>(stream));
 }
 

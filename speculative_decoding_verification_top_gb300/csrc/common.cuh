@@ -23,6 +23,7 @@ constexpr int kMinSeg = 2048;            // smallest warp segment (elements)
 constexpr int kSubW = 1024;              // elements per draw sub-tile (a warp)
 constexpr int kHistBins = 2048;          // top-p radix bins per pass (one CTA)
 constexpr int kElemCap = 1024;           // top-p select: logits of one histogram bin held in shared memory
+constexpr int kNucCap = 1024;            // top-p: nucleus list entries kept per row
 constexpr float kToppTry = 9.0f;         // top-p select: first try logits within 9 T of the max
 constexpr float kFix = 1099511627776.0f; // 2^40: fixed-point mass unit
 constexpr float kNegInf = -INFINITY;
@@ -58,7 +59,8 @@ struct SeqRec {         // one sequence's accept decision (and debug values)
     float pneg, pinv;  // -(m c) and 1/z of the draw's target row
     float qneg, qinv;  // the same for the draft row (residual only)
     uint32_t plam, qlam;  // nucleus keys of the two rows
-    uint32_t pad[2];
+    uint32_t done;     // the draw is already emitted (top-p nucleus list draw)
+    uint32_t pad;
     float P[32];       // p_i(x~_i)
     float Q[32];       // q_i(x~_i)
 };
@@ -72,6 +74,8 @@ struct Workspace {
     RowRec *rows;          // [rows]
     float *sub_sums;       // [B, NS] draw weight of every 1024-element sub-tile
     SeqRec *seqs;          // [B]
+    int32_t *nuc_n;        // [B (k+1)] entries of each target row's nucleus list, or -1 (top-p)
+    uint4 *nuc;            // [B (k+1), kNucCap] (index, target logit, draft logit at it), index order
     int pmax;              // partial slots per row
 };
 
@@ -299,6 +303,22 @@ struct Span {
     }
 };
 
+// Warp scan of one value per lane: exclusive prefix in lane order, and the
+// round total defined as (exclusive prefix of lane 31) + (its value).
+__device__ __forceinline__ float warp_excl_scan(float v, float &total) {
+    const int lane = threadIdx.x & 31;
+    float incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl = __fadd_rn(incl, y);
+    }
+    float excl = __shfl_up_sync(0xFFFFFFFFu, incl, 1);
+    if (lane == 0) excl = 0.0f;
+    total = __shfl_sync(0xFFFFFFFFu, __fadd_rn(excl, v), 31);
+    return excl;
+}
+
 // ------------------------------------------------- sequence completion
 
 // What the warp that finishes a sequence's last row does with it.
@@ -306,11 +326,108 @@ enum SeqWork { kSeqDecide = 0, kSeqGreedy = 1, kSeqNone = 2 };
 
 struct SeqArgs {
     int work;                    // SeqWork
+    int list_draw;               // draw from the rows' nucleus lists where they exist (top-p)
     const int32_t *draft_tokens; // [B, k]
     const float *uniforms;       // [B, k+1] (kSeqDecide)
     int32_t *out_tokens;         // [B, k+1]
     int32_t *out_num;            // [B]
 };
+
+// Weight of nucleus entry e of the draw row (index, target logit, draft
+// logit at that index): p(x), or max(0, p(x) - q(x)).
+template <typename T>
+__device__ __forceinline__ float list_weight(uint4 e, float c, bool use_p, float pneg, float pinv,
+                                             uint32_t plam, float qneg, float qinv,
+                                             uint32_t qlam) {
+    const float p = proc_prob<T>(__uint_as_float(e.y), c, pneg, pinv, plam);
+    if (use_p) return p;
+    const float q = proc_prob<T>(__uint_as_float(e.z), c, qneg, qinv, qlam);
+    return fmaxf(__fsub_rn(p, q), 0.0f);
+}
+
+// Total weight over a nucleus list: rounds of 32 entries in index order,
+// each round's total as warp_excl_scan defines it, folded in order.
+template <typename T>
+__device__ float list_total(const uint4 *L, int n, float c, bool use_p, float pneg, float pinv,
+                            uint32_t plam, float qneg, float qinv, uint32_t qlam) {
+    const int lane = threadIdx.x & 31;
+    float S = 0.0f;
+#pragma unroll 4
+    for (int r0 = 0; r0 < n; r0 += 32) {
+        const int i = r0 + lane;
+        const float w = i < n ? list_weight<T>(__ldcg(L + i), c, use_p, pneg, pinv, plam, qneg,
+                                               qinv, qlam)
+                              : 0.0f;
+        float rt;
+        warp_excl_scan(w, rt);
+        S = __fadd_rn(S, rt);
+    }
+    return S;
+}
+
+// The final draw of sequence b from the draw row's nucleus list (top-p):
+// every logit outside the target row's nucleus has p = 0, so the residual
+// max(0, p - q) and the bonus p both vanish there, and the inverse CDF in
+// index order runs over the list alone.  Same rule as the full-row draw:
+// the first entry with w > 0 whose cumulative weight exceeds u S (else the
+// last with w > 0); an empty residual draws from p instead.  Returns false
+// (nothing written) if the row has no list.
+template <typename T>
+__device__ bool list_draw(const RowView &v, const SeqArgs &sa, const Workspace &ws, float c,
+                          int b, int j, SeqRec *rec) {
+    const int lane = threadIdx.x & 31, k = v.k, R = 2 * k + 1;
+    const int tr = b * (k + 1) + j;  // the draw's target row among the target rows
+    const int n = __ldcg(&ws.nuc_n[tr]);
+    if (n < 0) return false;
+    const RowRec *rr = ws.rows + static_cast<size_t>(b) * R;
+    const RowRec *pr = rr + j;
+    const RowRec *qr = j < k ? rr + k + 1 + j : pr;
+    const float pneg = -__fmul_rn(__ldcg(&pr->m), c), pinv = __frcp_rn(__ldcg(&pr->z));
+    const float qneg = -__fmul_rn(__ldcg(&qr->m), c), qinv = __frcp_rn(__ldcg(&qr->z));
+    const uint32_t plam = __ldcg(&pr->lam_key), qlam = __ldcg(&qr->lam_key);
+    const uint4 *L = ws.nuc + static_cast<size_t>(tr) * kNucCap;
+    bool use_p = j == k;
+    float S = list_total<T>(L, n, c, use_p, pneg, pinv, plam, qneg, qinv, qlam);
+    if (!(S > 0.0f) && !use_p) {
+        use_p = true;
+        S = list_total<T>(L, n, c, use_p, pneg, pinv, plam, qneg, qinv, qlam);
+    }
+    const float target = __fmul_rn(sa.uniforms[static_cast<size_t>(b) * (k + 1) + k], S);
+    float Rsum = 0.0f;
+    int token = -1, lastpos = -1;
+    for (int r0 = 0; r0 < n && token < 0; r0 += 32) {
+        const int i = r0 + lane;
+        uint4 e = make_uint4(0u, 0u, 0u, 0u);
+        float w = 0.0f;
+        if (i < n) {
+            e = __ldcg(L + i);
+            w = list_weight<T>(e, c, use_p, pneg, pinv, plam, qneg, qinv, qlam);
+        }
+        float rt;
+        const float excl = warp_excl_scan(w, rt);
+        const bool hit = w > 0.0f && __fadd_rn(Rsum, __fadd_rn(excl, w)) > target;
+        const unsigned hm = __ballot_sync(0xFFFFFFFFu, hit);
+        if (hm) token = __shfl_sync(0xFFFFFFFFu, static_cast<int>(e.x), __ffs(hm) - 1);
+        const unsigned nz = __ballot_sync(0xFFFFFFFFu, w > 0.0f);
+        if (nz) lastpos = __shfl_sync(0xFFFFFFFFu, static_cast<int>(e.x), 31 - __clz(nz));
+        Rsum = __fadd_rn(Rsum, rt);
+    }
+    if (token < 0) token = lastpos;
+    int32_t *ot = sa.out_tokens + static_cast<size_t>(b) * (k + 1);
+    if (lane <= k) {
+        int32_t val = -1;
+        if (lane < j) val = sa.draft_tokens[static_cast<size_t>(b) * k + lane];
+        else if (lane == j) val = token;
+        ot[lane] = val;
+    }
+    if (lane == 0) {
+        sa.out_num[b] = j;
+        rec->S = S;
+        rec->use_p = use_p;
+        rec->done = 1u;
+    }
+    return true;
+}
 
 // Accept decisions of sequence b ("3.5 Speculative Decoding", step 3: for
 // i = 1..k accept x~_i iff u_i q_i(x~_i) < p_i(x~_i), stop at the first
@@ -372,6 +489,7 @@ __device__ void decide_sequence(const RowView &v, const SeqArgs &sa, const Works
         rec->qneg = -__fmul_rn(__ldcg(&qr->m), c);
         rec->qinv = __frcp_rn(__ldcg(&qr->z));
         rec->qlam = __ldcg(&qr->lam_key);
+        rec->done = 0u;
     }
     if (bad) {
         if (lane <= k) sa.out_tokens[static_cast<size_t>(b) * (k + 1) + lane] = -1;
@@ -379,6 +497,9 @@ __device__ void decide_sequence(const RowView &v, const SeqArgs &sa, const Works
             sa.out_num[b] = -1;
             atomicOr(ws.err, bad);
         }
+    } else if (sa.list_draw) {
+        __syncwarp();
+        list_draw<T>(v, sa, ws, c, b, j, rec);
     }
 }
 

@@ -121,22 +121,6 @@ __device__ __forceinline__ void weights(const Draw<T> &d, int x, int V, float c,
     weights_from<T>(d, x, V, c, lp, lq, w);
 }
 
-// Warp scan of one value per lane: exclusive prefix in lane order, and the
-// round total defined as (exclusive prefix of lane 31) + (its value).
-__device__ __forceinline__ float warp_excl_scan(float v, float &total) {
-    const int lane = threadIdx.x & 31;
-    float incl = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const float y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o) incl = __fadd_rn(incl, y);
-    }
-    float excl = __shfl_up_sync(0xFFFFFFFFu, incl, 1);
-    if (lane == 0) excl = 0.0f;
-    total = __shfl_sync(0xFFFFFFFFu, __fadd_rn(excl, v), 31);
-    return excl;
-}
-
 // Element order inside a 1024-element sub-tile: round u, then lane, then the
 // VE elements of the lane's vector -- exactly index order.
 template <typename T>
@@ -338,7 +322,7 @@ __device__ void finish_sequence(const FinalArgs &a, int b) {
     const int lane = threadIdx.x & 31, k = a.k, V = a.V;
     SeqRec *rec = a.ws.seqs + b;
     if (lane == 0) a.ws.seq_ctr[b] = 0u;
-    if (__ldcg(&rec->bad)) return;
+    if (__ldcg(&rec->bad) || __ldcg(&rec->done)) return;  // outputs already written
     Draw<T> d = make_draw<T>(a, b, rec);
     float *sums = a.ws.sub_sums + static_cast<size_t>(b) * a.NS;
     const float u = a.uniforms[static_cast<size_t>(b) * (k + 1) + k];
@@ -378,7 +362,7 @@ template <typename T>
 __device__ __forceinline__ void draw_run(const FinalArgs &a, int b, int t0, int t1) {
     const int lane = threadIdx.x & 31;
     const SeqRec *rec = a.ws.seqs + b;
-    if (!__ldcg(&rec->bad)) {
+    if (!__ldcg(&rec->bad) && !__ldcg(&rec->done)) {
         const Draw<T> d = make_draw<T>(a, b, rec);
         float *sums = a.ws.sub_sums + static_cast<size_t>(b) * a.NS;
         if constexpr (sizeof(T) == 2) {

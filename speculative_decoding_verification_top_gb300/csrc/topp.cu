@@ -123,18 +123,23 @@ struct ToppShared;
 struct ToppShared {
     SelShared sel;
     float alist[kAList];            // the logits pass A histogrammed (when they fit)
+    int aidx[kAList];               // ... and their indices in the row
     float elems[kElemCap];          // the logits of the crossing bin (pass B from global)
     float queue[kTpWarps][32 * 8];  // one vector slot of one warp (32 lanes x 8 logits)
+    int qidx[kTpWarps][32 * 8];     // ... and their indices in the row
+    int nidx[kElemCap];             // indices of the nucleus (list building)
     float pm[kTpWarps], ps[kTpWarps];
     uint32_t pf[kTpWarps];
     float m, Z;
     uint32_t flags;
-    int n_alist, n_elems;
+    uint32_t cmax;                  // running max of the row so far (ordered key)
+    int n_alist, n_elems, n_nuc;
     unsigned int kmin, kmax;
 };
 static_assert(sizeof(ToppShared) <= kToppSmem, "top-p shared memory");
 
-// Every logit >= vmin of a row from global memory, calling `f(l)` on each.
+// Every logit >= vmin of a row from global memory, calling `f(l, x)` on
+// each (x: its index in the row).
 // Warp w streams the w-th eighth of the row's 16-byte vectors (kBatch per
 // lane in flight, the next batch loaded while this one is reduced).  For
 // every vector slot of a batch the warp first packs its logits >= vmin into
@@ -146,14 +151,15 @@ __device__ __forceinline__ void for_row(ToppShared &sh, const T *rowp, int V, fl
     constexpr int P = Elem<T>::kPerVec;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     float *q_w = sh.queue[warp];
+    int *qi_w = sh.qidx[warp];
     const Span<T> sp(rowp, 0, V);
     if (tid < sp.a0 - sp.e0) {
         const float l = to_f32(rowp[sp.e0 + tid]);
-        if (l >= vmin) f(l);
+        if (l >= vmin) f(l, sp.e0 + tid);
     }
     if (tid < sp.e1 - sp.a1) {
         const float l = to_f32(rowp[sp.a1 + tid]);
-        if (l >= vmin) f(l);
+        if (l >= vmin) f(l, sp.a1 + tid);
     }
     const int per = (sp.nvec + kTpWarps - 1) / kTpWarps;
     const int v0w = min(sp.nvec, warp * per), n = min(sp.nvec, v0w + per) - v0w;
@@ -191,16 +197,182 @@ __device__ __forceinline__ void for_row(ToppShared &sh, const T *rowp, int V, fl
             }
             const int tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
             int pos = incl - cnt;
+            const int x0 = sp.a0 + (v0w + b0 + u * 32 + lane) * P;
 #pragma unroll
             for (int e = 0; e < P; ++e)
-                if (mask & (1u << e)) q_w[pos++] = h[e];
+                if (mask & (1u << e)) {
+                    q_w[pos] = h[e];
+                    qi_w[pos] = x0 + e;
+                    ++pos;
+                }
             __syncwarp();
-            for (int i = lane; i < tot; i += 32) f(q_w[i]);
+            for (int i = lane; i < tot; i += 32) f(q_w[i], qi_w[i]);
             __syncwarp();
         }
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) q[u] = nq[u];
     }
+}
+
+// Append, for a whole warp, each lane's logits h[e] with bit e of `mask`
+// set (indices x0 + e) to the pass-A list: one shared atomic per warp.
+template <int N>
+__device__ __forceinline__ void alist_append(ToppShared &sh, uint32_t mask, const float (&h)[N],
+                                             int x0) {
+    const int lane = threadIdx.x & 31;
+    if (!__ballot_sync(0xFFFFFFFFu, mask != 0u)) return;
+    const int cnt = __popc(mask);
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    const int tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    int base = 0;
+    if (lane == 31) base = atomicAdd(&sh.n_alist, tot);
+    base = __shfl_sync(0xFFFFFFFFu, base, 31);
+    int pos = base + incl - cnt;
+#pragma unroll
+    for (int e = 0; e < N; ++e)
+        if (mask & (1u << e)) {
+            if (pos < kAList) {
+                sh.alist[pos] = h[e];
+                sh.aidx[pos] = x0 + e;
+            }
+            ++pos;
+        }
+}
+
+// alist_append for one batch of kBatch vectors per lane: element u P + e
+// of a lane lies at index x0 + u 32 P + e.
+template <int P>
+__device__ __forceinline__ void alist_append_batch(ToppShared &sh, uint32_t mask,
+                                                   const float (&h)[kBatch * P], int x0) {
+    const int lane = threadIdx.x & 31;
+    if (!__ballot_sync(0xFFFFFFFFu, mask != 0u)) return;
+    const int cnt = __popc(mask);
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    const int tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    int base = 0;
+    if (lane == 31) base = atomicAdd(&sh.n_alist, tot);
+    base = __shfl_sync(0xFFFFFFFFu, base, 31);
+    int pos = base + incl - cnt;
+#pragma unroll
+    for (int i = 0; i < kBatch * P; ++i)
+        if (mask & (1u << i)) {
+            if (pos < kAList) {
+                sh.alist[pos] = h[i];
+                sh.aidx[pos] = x0 + (i / P) * 32 * P + (i % P);
+            }
+            ++pos;
+        }
+}
+
+// The float whose okey<float> is k.
+__device__ __forceinline__ float key_float(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// Statistics of the piece [lo, hi) of the row into this lane's (m_run,
+// s_run), as warp_piece_ms computes them, and meanwhile every logit >= (the
+// CTA's running max) - tryT appended to the pass-A list: the running max
+// never exceeds the row's max m, so every logit >= m - tryT is appended
+// (those the list can hold).
+template <typename T>
+__device__ __forceinline__ void stats_capture(ToppShared &sh, const T *rowp, int lo, int hi,
+                                              float c, float tryT, float &m_run, float &s_run,
+                                              uint32_t &fl) {
+    constexpr int P = Elem<T>::kPerVec;
+    const int lane = threadIdx.x & 31;
+    const Span<T> sp(rowp, lo, hi);
+    auto scalar = [&](float l) {
+        if (l != l) {
+            fl |= kFlagNonFinite;
+            return;
+        }
+        if (l > m_run) {
+            s_run = __fmul_rn(s_run, ex2(__fmul_rn(__fsub_rn(m_run, l), c)));
+            m_run = l;
+        }
+        if (m_run != kNegInf)
+            s_run = __fadd_rn(s_run, ex2(__fmaf_rn(l, c, -__fmul_rn(m_run, c))));
+    };
+    // Threshold from the warp's and the CTA's running max.
+    auto floor_now = [&]() {
+        float wm = m_run;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xFFFFFFFFu, wm, o));
+        uint32_t ck = wm > kNegInf ? okey<float>(wm) : 0u;
+        if (lane == 0 && ck) ck = max(ck, atomicMax(&sh.cmax, ck));
+        ck = __shfl_sync(0xFFFFFFFFu, ck, 0);
+        return ck ? __fsub_rn(key_float(ck), tryT) : INFINITY;
+    };
+    // The ragged ends (< one vector each): counted, then appended if >= the floor.
+    auto edge = [&](int n0, int n1) {
+        float h[1] = {kNegInf};
+        if (lane < n1 - n0) {
+            h[0] = to_f32(rowp[n0 + lane]);
+            scalar(h[0]);
+        }
+        const float fl_now = floor_now();
+        alist_append<1>(sh, (h[0] >= fl_now && h[0] > kNegInf) ? 1u : 0u, h, n0 + lane);
+    };
+    edge(sp.e0, sp.a0);
+    const uint4 *vp = reinterpret_cast<const uint4 *>(rowp + sp.a0);
+    const uint4 neg = neg_inf_vec<T>();
+    constexpr int kStride = 32 * kBatch;
+    uint4 q[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) q[u] = lane + u * 32 < sp.nvec ? ld_stream(vp + lane + u * 32) : neg;
+    for (int v0 = 0; v0 < sp.nvec; v0 += kStride) {  // warp-uniform trip count
+        uint4 nq[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int v = v0 + kStride + u * 32 + lane;
+            nq[u] = v < sp.nvec ? ld_stream(vp + v) : neg;
+        }
+        const float bm = batch_max<T>(q);
+        const bool nan = bm != bm;
+        if (nan) fl |= kFlagNonFinite;
+        else if (bm > m_run) {
+            s_run = __fmul_rn(s_run, ex2(__fmul_rn(__fsub_rn(m_run, bm), c)));
+            m_run = bm;
+        }
+        // Floor after this batch's max is counted (so the batch's own top
+        // logits are kept); one unpack feeds the sum and the capture mask.
+        const float thr = floor_now();
+        const bool sum = !nan && m_run != kNegInf;
+        const float negmc = -__fmul_rn(m_run, c);
+        float acc0 = 0.0f, acc1 = 0.0f;
+        float h[kBatch * P];
+        uint32_t mask = 0u;
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            float f[P];
+            unpack<T>(q[u], f);
+#pragma unroll
+            for (int e = 0; e < P; e += 2) {
+                acc0 = __fadd_rn(acc0, ex2(__fmaf_rn(f[e], c, negmc)));
+                acc1 = __fadd_rn(acc1, ex2(__fmaf_rn(f[e + 1], c, negmc)));
+            }
+#pragma unroll
+            for (int e = 0; e < P; ++e) {
+                h[u * P + e] = f[e];
+                if (f[e] >= thr && f[e] > kNegInf) mask |= 1u << (u * P + e);
+            }
+        }
+        if (sum) s_run = __fadd_rn(s_run, __fadd_rn(acc0, acc1));
+        alist_append_batch<P>(sh, mask, h, sp.a0 + (v0 + lane) * P);
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) q[u] = nq[u];
+    }
+    edge(sp.a1, sp.e1);
 }
 
 template <typename T>
@@ -213,15 +385,22 @@ __global__ void __launch_bounds__(kTpThreads, 3) topp_kernel(const ToppArgs a) {
     const int row = blockIdx.x, tid = threadIdx.x;
     RowRec *rec = a.ws.rows + row;
     const T *rowp = row_ptr<T>(a.rows, row);
+    const float tryT = kToppTry * a.temperature;
     {
         // Row statistics: warp w reduces the w-th eighth of the row (a
-        // split fixed by V alone), combined in warp order.
+        // split fixed by V alone), combined in warp order; the logits near
+        // the running max are kept for the select.
         const int V = a.rows.V, warp = tid >> 5;
         const int per = ((V + kTpWarps - 1) / kTpWarps + 7) / 8 * 8;
         const int lo = min(V, warp * per), hi = min(V, lo + per);
+        if (tid == 0) {
+            sh.n_alist = 0;
+            sh.cmax = 0u;
+        }
+        __syncthreads();
         float pm = kNegInf, ps = 0.0f;
         uint32_t pf = 0u;
-        warp_piece_ms<T>(rowp, lo, hi, a.c, pm, ps, pf);
+        stats_capture<T>(sh, rowp, lo, hi, a.c, tryT, pm, ps, pf);
         warp_reduce_ms(pm, ps, pf, a.c);
         if ((tid & 31) == 0) {
             sh.pm[warp] = pm;
@@ -261,7 +440,10 @@ __global__ void __launch_bounds__(kTpThreads, 3) topp_kernel(const ToppArgs a) {
         // If the mass of the logits >= y1 already reaches top_p Z the
         // crossing bin is found there (exactly: the histogram holds every
         // logit >= y1); otherwise pass A runs again over [c0, m].
-        float lo = fmaxf(cut, m - kToppTry * a.temperature);
+        float lo = fmaxf(cut, m - tryT);
+        // The statistics pass kept every logit >= m - tryT (its floors never
+        // exceed that), so every logit >= lo, unless the list overflowed.
+        const bool from_list = sh.n_alist <= kAList;
         float span = 0.0f, inv = 0.0f;
         auto vbin = [&](float l) {
             return min(static_cast<int>(__fmul_rn(__fsub_rn(m, l), inv)), kHistBins - 1);
@@ -275,13 +457,26 @@ __global__ void __launch_bounds__(kTpThreads, 3) topp_kernel(const ToppArgs a) {
             span = __fsub_rn(m, lo);
             inv = span > 0.0f ? static_cast<float>(kHistBins) / span : 0.0f;
             cta_clear(sh.sel);
-            if (tid == 0) sh.n_alist = 0;
-            __syncthreads();
-            for_row<T>(sh, rowp, V, lo, [&](float l) {
-                atomicAdd(&sh.sel.hist[vbin(l)], mass(l));
-                const int pos = atomicAdd(&sh.n_alist, 1);
-                if (pos < kAList) sh.alist[pos] = l;
-            });
+            if (attempt == 0 && from_list) {
+                const int na0 = sh.n_alist;
+                for (int i = tid; i < na0; i += kTpThreads) {
+                    const float l = sh.alist[i];
+                    if (l >= lo) atomicAdd(&sh.sel.hist[vbin(l)], mass(l));
+                }
+            } else {
+                // From the row: pass A again (it mostly hits L2), keeping
+                // the logits >= lo.
+                if (tid == 0) sh.n_alist = 0;
+                __syncthreads();
+                for_row<T>(sh, rowp, V, lo, [&](float l, int x) {
+                    atomicAdd(&sh.sel.hist[vbin(l)], mass(l));
+                    const int pos = atomicAdd(&sh.n_alist, 1);
+                    if (pos < kAList) {
+                        sh.alist[pos] = l;
+                        sh.aidx[pos] = x;
+                    }
+                });
+            }
             __syncthreads();
             bool crossed;
             b0 = cta_cross(sh.sel, kHistBins, 0ull, tgt, &above, &hb, &crossed);
@@ -303,7 +498,7 @@ __global__ void __launch_bounds__(kTpThreads, 3) topp_kernel(const ToppArgs a) {
         }
         __syncthreads();
         const int na = sh.n_alist;
-        auto take = [&](float l) {
+        auto take = [&](float l, int) {
             if (l >= lo && vbin(l) == b0) {
                 const int pos = atomicAdd(&sh.n_elems, 1);
                 if (pos < kElemCap) sh.elems[pos] = l;
@@ -312,7 +507,7 @@ __global__ void __launch_bounds__(kTpThreads, 3) topp_kernel(const ToppArgs a) {
             }
         };
         if (na <= kAList) {
-            for (int i = tid; i < na; i += kTpThreads) take(sh.alist[i]);
+            for (int i = tid; i < na; i += kTpThreads) take(sh.alist[i], 0);
         } else {
             for_row<T>(sh, rowp, V, vmin, take);
         }
@@ -335,7 +530,7 @@ __global__ void __launch_bounds__(kTpThreads, 3) topp_kernel(const ToppArgs a) {
             if (ne <= kElemCap) {
                 for (int i = tid; i < ne; i += kTpThreads) add(sh.elems[i]);
             } else {
-                for_row<T>(sh, rowp, V, vmin, [&](float l) {
+                for_row<T>(sh, rowp, V, vmin, [&](float l, int) {
                     if (l >= lo && vbin(l) == b0) add(l);
                 });
             }
@@ -353,6 +548,51 @@ __global__ void __launch_bounds__(kTpThreads, 3) topp_kernel(const ToppArgs a) {
         }
         lam = khi;
         zk = __fmul_rn(__ull2float_rn(khi == klo ? above + hb : tgt), 1.0f / kFix);
+        // The nucleus list of a target row for the final draw: the kept
+        // logits (keys >= lam, all of them >= lo, so all in pass A's list
+        // when it did not overflow), ranked by index, each with the draft
+        // logit at the same index (row r's residual pairs target row r
+        // with draft row r; the bonus row has no draft row).
+        const int R = a.rows.R, kk = a.rows.k;
+        const int bq = row / R, rq = row - bq * R;
+        if (a.seq.list_draw && rq <= kk) {
+            if (tid == 0) sh.n_nuc = 0;
+            __syncthreads();
+            const int na2 = sh.n_alist;
+            if (na2 <= kAList) {
+                for (int i = tid; i < na2; i += kTpThreads)
+                    if (okey<T>(sh.alist[i]) >= lam) {
+                        const int pos = atomicAdd(&sh.n_nuc, 1);
+                        if (pos < kElemCap) {
+                            sh.elems[pos] = sh.alist[i];
+                            sh.nidx[pos] = sh.aidx[i];
+                        }
+                    }
+            }
+            __syncthreads();
+            const int nn = sh.n_nuc;
+            const bool ok = na2 <= kAList && nn <= min(kElemCap, kNucCap);
+            const int tr = bq * (kk + 1) + rq;
+            uint4 *L = a.ws.nuc + static_cast<size_t>(tr) * kNucCap;
+            const T *drow = rq < kk ? static_cast<const T *>(a.rows.draft) +
+                                          (static_cast<size_t>(bq) * kk + rq) * V
+                                    : nullptr;
+            if (ok) {
+                const int *ix = sh.nidx;
+                for (int i = tid; i < nn; i += kTpThreads) {
+                    const int xi = ix[i];
+                    int rank = 0;
+                    for (int t = 0; t < nn; ++t) rank += ix[t] < xi;
+                    const float lq = drow ? to_f32(drow[xi]) : 0.0f;
+                    L[rank] = make_uint4(static_cast<uint32_t>(xi), __float_as_uint(sh.elems[i]),
+                                         __float_as_uint(lq), 0u);
+                }
+            }
+            if (tid == 0) a.ws.nuc_n[tr] = ok ? nn : -1;
+        }
+    } else if (tid == 0 && a.seq.list_draw) {
+        const int R = a.rows.R, kk = a.rows.k, bq = row / R, rq = row - bq * R;
+        if (rq <= kk) a.ws.nuc_n[bq * (kk + 1) + rq] = -1;
     }
     if (tid == 0) {
         RowRec r;
@@ -365,6 +605,7 @@ __global__ void __launch_bounds__(kTpThreads, 3) topp_kernel(const ToppArgs a) {
         r.pad[0] = r.pad[1] = 0;
         *rec = r;
     }
+    __threadfence();  // the nucleus list, for whichever warp decides the sequence
     __syncthreads();
     if (tid < 32) row_done<T>(a.rows, a.seq, a.ws, a.c, row);
 }
