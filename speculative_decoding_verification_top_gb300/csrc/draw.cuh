@@ -356,8 +356,7 @@ __device__ void finish_sequence(const FinalArgs &a, int b) {
 
 // Sum sub-tiles [t0, t1) of sequence b's draw into its sub-tile sums and
 // report them; the last report finishes the sequence.  A sequence with a
-// data error reports without summing.  For bf16 the next sub-tile's loads
-// are in flight while the current one is reduced.
+// data error, or already drawn, reports without summing.
 template <typename T>
 __device__ __forceinline__ void draw_run(const FinalArgs &a, int b, int t0, int t1) {
     const int lane = threadIdx.x & 31;
@@ -365,20 +364,9 @@ __device__ __forceinline__ void draw_run(const FinalArgs &a, int b, int t0, int 
     if (!__ldcg(&rec->bad) && !__ldcg(&rec->done)) {
         const Draw<T> d = make_draw<T>(a, b, rec);
         float *sums = a.ws.sub_sums + static_cast<size_t>(b) * a.NS;
-        if constexpr (sizeof(T) == 2) {
-            SubLoad<T> cur, nxt;
-            subtile_load<T>(d, t0, a.V, cur);
-            for (int t = t0; t < t1; ++t) {
-                if (t + 1 < t1) subtile_load<T>(d, t + 1, a.V, nxt);
-                const float tot = subtile_reduce<T>(d, t, a.V, a.c, cur);
-                if (lane == 0) sums[t] = tot;
-                cur = nxt;
-            }
-        } else {
-            for (int t = t0; t < t1; ++t) {
-                const float tot = subtile_total<T>(d, t, a.V, a.c);
-                if (lane == 0) sums[t] = tot;
-            }
+        for (int t = t0; t < t1; ++t) {
+            const float tot = subtile_total<T>(d, t, a.V, a.c);
+            if (lane == 0) sums[t] = tot;
         }
     }
     int last = 0;

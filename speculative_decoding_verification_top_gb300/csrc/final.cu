@@ -23,7 +23,7 @@ namespace {
 // Persistent grid: warp w sums its even share of the sub-tiles in the
 // flattened (sequence, sub-tile) order, and reports them once per sequence.
 template <typename T>
-__global__ void __launch_bounds__(kThreads, 2) final_kernel(const FinalArgs a) {
+__global__ void __launch_bounds__(kThreads, sizeof(T) == 2 ? 3 : 2) final_kernel(const FinalArgs a) {
     // Wait until the row kernel has finished and its writes are visible.
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const long long w = static_cast<long long>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
