@@ -60,18 +60,20 @@ __device__ __forceinline__ void warp_piece_ms(const T *rowp, int lo, int hi, flo
             }
             if (m_run != kNegInf) {
                 const float negmc = -__fmul_rn(m_run, c);
-                float acc0 = 0.0f, acc1 = 0.0f;
+                float2 acc = make_float2(0.0f, 0.0f);
 #pragma unroll
                 for (int u = 0; u < kBatch; ++u) {
                     float f[P];
                     unpack<T>(q[u], f);
 #pragma unroll
                     for (int e = 0; e < P; e += 2) {
-                        acc0 = __fadd_rn(acc0, ex2(__fmaf_rn(f[e], c, negmc)));
-                        acc1 = __fadd_rn(acc1, ex2(__fmaf_rn(f[e + 1], c, negmc)));
+                        // even logits into acc.x, odd into acc.y
+                        const float2 x = fma2(make_float2(f[e], f[e + 1]), make_float2(c, c),
+                                              make_float2(negmc, negmc));
+                        acc = add2(acc, make_float2(ex2(x.x), ex2(x.y)));
                     }
                 }
-                s_run = __fadd_rn(s_run, __fadd_rn(acc0, acc1));
+                s_run = __fadd_rn(s_run, __fadd_rn(acc.x, acc.y));
             }
         }
 #pragma unroll

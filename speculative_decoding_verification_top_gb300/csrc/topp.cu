@@ -349,7 +349,7 @@ __device__ __forceinline__ void stats_capture(ToppShared &sh, const T *rowp, int
         const float thr = floor_now();
         const bool sum = !nan && m_run != kNegInf;
         const float negmc = -__fmul_rn(m_run, c);
-        float acc0 = 0.0f, acc1 = 0.0f;
+        float2 acc = make_float2(0.0f, 0.0f);
         float h[kBatch * P];
         uint32_t mask = 0u;
 #pragma unroll
@@ -358,8 +358,9 @@ __device__ __forceinline__ void stats_capture(ToppShared &sh, const T *rowp, int
             unpack<T>(q[u], f);
 #pragma unroll
             for (int e = 0; e < P; e += 2) {
-                acc0 = __fadd_rn(acc0, ex2(__fmaf_rn(f[e], c, negmc)));
-                acc1 = __fadd_rn(acc1, ex2(__fmaf_rn(f[e + 1], c, negmc)));
+                const float2 x = fma2(make_float2(f[e], f[e + 1]), make_float2(c, c),
+                                      make_float2(negmc, negmc));
+                acc = add2(acc, make_float2(ex2(x.x), ex2(x.y)));
             }
 #pragma unroll
             for (int e = 0; e < P; ++e) {
@@ -367,7 +368,7 @@ __device__ __forceinline__ void stats_capture(ToppShared &sh, const T *rowp, int
                 if (f[e] >= thr && f[e] > kNegInf) mask |= 1u << (u * P + e);
             }
         }
-        if (sum) s_run = __fadd_rn(s_run, __fadd_rn(acc0, acc1));
+        if (sum) s_run = __fadd_rn(s_run, __fadd_rn(acc.x, acc.y));
         alist_append_batch<P>(sh, mask, h, sp.a0 + (v0 + lane) * P);
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) q[u] = nq[u];
