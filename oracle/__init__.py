@@ -69,6 +69,8 @@ def _load():
         lib.oracle_inverse_cdf.restype = ctypes.c_int32
         lib.oracle_verify_sample.argtypes = [P, P, I, P, P, I, I, I, D, D, I, P, P, P, P]
         lib.oracle_verify_sample.restype = I
+        lib.oracle_acceptance.argtypes = [P, P, I, I, I, I, D, D, P, P]
+        lib.oracle_acceptance.restype = I
         lib.oracle_ancestor_mask.argtypes = [P, I, P]
         lib.oracle_ancestor_mask.restype = I
         lib.oracle_verify_tree.argtypes = [P, I, P, P, I, I, I, I, P, P, P]
@@ -153,6 +155,26 @@ def verify_sample(target, draft, draft_tokens, uniforms, T=1.0, top_p=1.0, mode=
     if debug:
         res.update(dbg=dbg, row_info=info)
     return res
+
+
+def acceptance(target, draft, T=1.0, top_p=1.0):
+    """Per-position acceptance rate beta [B, k] = sum_x min(p_i, q_i) and
+    total-variation distance tv [B, k] = (1/2) sum_x |p_i - q_i|, each from
+    its own definition.  target [B, k+1, V], draft [B, k, V].
+    Returns dict(beta, tv, errors); NaN marks a pair with a data error."""
+    tgt, dt = _logits(target)
+    drf, dt2 = _logits(draft)
+    B, k1, V = tgt.shape
+    k = k1 - 1
+    if dt2 != dt or drf.shape != (B, k, V):
+        raise ValueError("draft logits must match target dtype and be [B, k, V]")
+    beta = np.zeros((B, k), np.float64)
+    tv = np.zeros((B, k), np.float64)
+    err = _load().oracle_acceptance(_ptr(tgt), _ptr(drf), dt, B, k, V, float(T), float(top_p),
+                                    _ptr(beta), _ptr(tv))
+    if err < 0:
+        raise ValueError("oracle_acceptance rejected its arguments")
+    return dict(beta=beta, tv=tv, errors=err)
 
 
 def ancestor_mask(parents):

@@ -14,7 +14,8 @@
  *        for one token", 3.1 "The acceptance step", 3.3 "The full block loop".
  *   [LB] "Speculative Decoding: Mathematical Foundations, Rejection Sampling
  *        Dynamics, ..." (llms.blog): "The Modified Rejection Sampling
- *        Algorithm", "Tree-Based Verification and Custom Attention Masks".
+ *        Algorithm", "Acceptance Rate and Total Variation Distance",
+ *        "Tree-Based Verification and Custom Attention Masks".
  *   [SS] "Speculative Decoding from First Principles" (theservingstack.com):
  *        "Draft, verify, keep what matches".
  *
@@ -386,6 +387,63 @@ int oracle_verify_sample(const void *target, const void *draft, int dtype,
     free(prob);
     free(w);
     free(g);
+    return errors;
+}
+
+/* ------------------------------------------------------ acceptance rate */
+
+/*
+ * Per-position acceptance rate and total-variation distance of one
+ * verification batch.  [LZ] "Proof that the output distribution is exactly
+ * p": the chance that position i accepts (given that it is tested) is
+ * beta_i = sum_x min(p_i(x), q_i(x)), one minus the total-variation
+ * distance; [LB] "Acceptance Rate and Total Variation Distance" defines
+ * TV(p, q) = (1/2) sum_x |p(x) - q(x)|; [MN] 3.2 measures the rate as
+ * sum_t min(p_t, q_t).  Both sums are taken here straight from their
+ * definitions, in token order, over p_i and q_i processed exactly as in
+ * oracle_verify_sample; neither is derived from the other.
+ *
+ * target [B, k+1, V] (rows 0..k-1 used), draft [B, k, V]
+ * beta [B, k], tv [B, k] (tv may be NULL): NaN where either row of the pair
+ *      has a data error (R7)
+ * Returns ORC_BAD_ARGUMENT, or the OR of (1 << status) over failed rows.
+ */
+int oracle_acceptance(const void *target, const void *draft, int dtype,
+                      int B, int k, int V, double T, double top_p,
+                      double *beta, double *tv)
+{
+    if (!target || !draft || !beta || B < 0 || k < 1 || V < 1 ||
+        (dtype != ORC_F32 && dtype != ORC_BF16) || !(T > 0.0) ||
+        !(top_p > 0.0) || top_p > 1.0)
+        return ORC_BAD_ARGUMENT;
+    const size_t esz = dtype == ORC_F32 ? 4 : 2;
+    double *p = (double *)malloc((size_t)V * sizeof *p);
+    double *q = (double *)malloc((size_t)V * sizeof *q);
+    int errors = 0;
+    for (int b = 0; b < B; ++b) {
+        for (int i = 0; i < k; ++i) {
+            const char *prow = (const char *)target + ((size_t)b * (k + 1) + i) * V * esz;
+            const char *qrow = (const char *)draft + ((size_t)b * k + i) * V * esz;
+            int sp = oracle_process_row(prow, dtype, V, T, top_p, p, NULL);
+            int sq = oracle_process_row(qrow, dtype, V, T, top_p, q, NULL);
+            double overlap = NAN, dist = NAN;
+            if (sp != ORC_OK) errors |= 1 << sp;
+            if (sq != ORC_OK) errors |= 1 << sq;
+            if (sp == ORC_OK && sq == ORC_OK) {
+                overlap = 0.0;
+                dist = 0.0;
+                for (int x = 0; x < V; ++x) {
+                    overlap += p[x] < q[x] ? p[x] : q[x];
+                    dist += fabs(p[x] - q[x]);
+                }
+                dist *= 0.5;
+            }
+            beta[(size_t)b * k + i] = overlap;
+            if (tv) tv[(size_t)b * k + i] = dist;
+        }
+    }
+    free(p);
+    free(q);
     return errors;
 }
 
