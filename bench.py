@@ -244,11 +244,30 @@ class Job:
         else:
             sv.spec_verify_sample(*self.chain_args(i))
 
-    def rows_only(self, i, ev_a, ev_b):
-        """The row kernel of one chain step alone, between two events."""
-        ev_a.record(self.stream)
+    def rows_only(self, i):
+        """The row phase of one chain step alone."""
         self.sv.spec_verify_sample_rows(*self.chain_args(i))
-        ev_b.record(self.stream)
+
+
+def device_launch_ms(launch, n, stream, chunk=100):
+    """Mean device time of launch(i), i < n, each bracketed by CUDA events on
+    `stream`.  Each chunk of launches is queued behind a ~25 ms device-side
+    sleep, so the host is far ahead when they run: the events time the
+    kernels back to back, not the host's launch latency."""
+    import torch
+    times = []
+    for c0 in range(0, n, chunk):
+        m = min(chunk, n - c0)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(m)]
+        torch.cuda._sleep(50_000_000)
+        for j, (a, b) in enumerate(evs):
+            a.record(stream)
+            launch(c0 + j)
+            b.record(stream)
+        torch.cuda.synchronize()
+        times += [a.elapsed_time(b) for a, b in evs]
+    return float(np.mean(times))
 
 
 def timed_device(job, steps, warmup, world, kernel_launches=500):
@@ -271,19 +290,47 @@ def timed_device(job, steps, warmup, world, kernel_launches=500):
     total_ms = ev0.elapsed_time(ev1)
     rows_ms = None
     if job.mode != "tree":
-        n = min(steps, kernel_launches)
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(n)]
         for i in range(3):
-            job.rows_only(i, *evs[0])
+            job.rows_only(i)
         torch.cuda.synchronize()
-        for i, (a, b) in enumerate(evs):
-            job.rows_only(i, a, b)
-        torch.cuda.synchronize()
-        rows_ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
+        rows_ms = device_launch_ms(job.rows_only, min(steps, kernel_launches), job.stream)
         job.step(0)  # leave the workspace as a finished call left it
         torch.cuda.synchronize()
     return total_ms, rows_ms
+
+
+def timed_acceptance(job, launches=200):
+    """spec_verify_acceptance on the finished call's workspace: launches
+    bracketed by events, alternating the two (identical) input copies so
+    that consecutive launches do not find their rows in L2."""
+    import torch
+    wl, sv = job.wl, job.sv
+    beta = torch.empty((wl.B, wl.k), dtype=torch.float32, device=job.dev)
+    tv = torch.empty((wl.B, wl.k), dtype=torch.float32, device=job.dev)
+
+    def one(i):
+        t, d = job.sets[i % 2][:2]
+        sv.spec_verify_acceptance(t.data_ptr(), d.data_ptr(), wl.B, wl.k, wl.V, wl.T, wl.top_p,
+                                  job.dtype, beta.data_ptr(), tv.data_ptr(), job.ws.data_ptr(),
+                                  job.ws.numel(), job.stream.cuda_stream)
+
+    for i in range(3):
+        one(i)
+    torch.cuda.synchronize()
+    ms = device_launch_ms(one, launches, job.stream)
+    esz = 2 if wl.dtype == workloads.BF16 else 4
+    listed = wl.top_p < 1.0
+    # Without top-p both rows of every pair are read once; with top-p the
+    # pairs are summed over the nucleus lists (no row is read when every
+    # list fits), so no byte count is claimed.
+    nbytes = None if listed else 2 * wl.B * wl.k * wl.V * esz
+    out = {"kernel": "accept_kernel", "launches": launches, "avg_launch_us": round(ms * 1e3, 2),
+           "mean_beta": round(float(beta.double().mean().item()), 5),
+           "path": "nucleus lists" if listed else "both rows streamed"}
+    if nbytes:
+        out["algorithmic_bytes"] = nbytes
+        out["achieved_gbs"] = round(nbytes / (ms * 1e-3) / 1e9, 1)
+    return out
 
 
 def timed_e2e(job, steps):
@@ -374,6 +421,7 @@ def run_ours(args):
     time.sleep(0.3)
     total_ms, rows_ms = timed_device(job, args.steps, args.warmup, world)
     clk = clocks.stop()
+    accept = timed_acceptance(job) if mode != "tree" else None
     total_ms = max_over_ranks(total_ms, world)
 
     nbytes = wl.logit_bytes(mode)
@@ -422,6 +470,10 @@ def run_ours(args):
         "gpu_launches": job.launches_per_step * args.steps,
         "clocks": clk,
     }
+    if accept is not None:
+        if "achieved_gbs" in accept:
+            accept["frac"] = round(accept["achieved_gbs"] / peak, 4)
+        out["acceptance"] = accept
     if rank == 0 and world == 1:
         out["cpu_baseline"] = cpu_baseline(wl, mode, args.cpu_seconds)
     if rank == 0:

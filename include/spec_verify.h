@@ -251,6 +251,37 @@ int spec_verify_intermediates(const void *workspace, size_t workspace_bytes,
                               int B, int k, int V, float *P, float *Q, float *Z,
                               float *S, spec_stream_t stream);
 
+/*
+ * Per-position acceptance rate of the last verification step -- [LZ]
+ * "Proof that the output distribution is exactly p": once position i is
+ * tested it accepts with probability
+ *   beta_i = sum_x min(p_i(x), q_i(x)) = 1 - TV(p_i, q_i),
+ * and [LB] "Acceptance Rate and Total Variation Distance": TV(p, q) =
+ * (1/2) sum_x |p(x) - q(x)|.  Engines log beta to track how well the draft
+ * matches the target.
+ *
+ * Reads the per-row statistics that the last spec_verify_sample (or
+ * spec_verify_sample_rows) call left in `workspace`; that call must have
+ * been SPEC_STOCHASTIC, with the same target_logits, draft_logits, B, k,
+ * V, temperature, top_p and dtype, on this stream (or ordered before it).
+ * Otherwise the results are meaningless (never out of bounds).  It changes
+ * nothing that spec_verify_sample_finish reads, so it may run between
+ * _rows and _finish.
+ *
+ * Arguments
+ *   target_logits, draft_logits, B, k, V, temperature, top_p, dtype: as for
+ *                    spec_verify_sample (target rows k+1 are not read)
+ *   out_beta         [B, k] fp32, device: beta_i for i = 1..k; NaN where
+ *                    row i of the target or draft has a data error
+ *   out_tv           [B, k] fp32, device, or NULL: 1 - beta_i
+ *   workspace        the verify call's workspace
+ * Returns SPEC_OK or a negative status; nothing is enqueued on error.
+ */
+int spec_verify_acceptance(const void *target_logits, const void *draft_logits, int B,
+                           int k, int V, float temperature, float top_p, int dtype,
+                           float *out_beta, float *out_tv, void *workspace,
+                           size_t workspace_bytes, spec_stream_t stream);
+
 /* Static, human-readable description of a status or data-error bit. */
 const char *spec_verify_status_string(int status);
 

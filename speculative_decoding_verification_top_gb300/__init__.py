@@ -10,8 +10,9 @@ Entry points (same names as the C ABI):
     spec_verify_workspace_size, spec_verify_tree_workspace_size,
     spec_verify_workspace_init, spec_verify_sample, spec_verify_tree,
     spec_verify_last_error, spec_verify_intermediates,
-    spec_verify_status_string
-plus tensor-level helpers ``verify_sample`` / ``verify_tree`` that take
+    spec_verify_acceptance, spec_verify_status_string
+plus tensor-level helpers ``verify_sample`` / ``verify_tree`` /
+``acceptance`` that take
 torch CUDA tensors, allocate outputs and a zeroed workspace, and raise on a
 negative status.
 """
@@ -26,7 +27,8 @@ _ROOT = os.path.dirname(_PKG)
 LIB_PATH = os.path.join(_PKG, "libspecverify.so")
 CSRC = os.path.join(_PKG, "csrc")
 SOURCES = [os.path.join(CSRC, f)
-           for f in ("api.cu", "rows.cu", "topp.cu", "final.cu", "noalloc.cu")]
+           for f in ("api.cu", "rows.cu", "topp.cu", "final.cu", "noalloc.cu",
+                     "accept.cu")]
 HEADERS = [os.path.join(CSRC, f) for f in ("common.cuh", "stream.cuh", "draw.cuh")]
 INCLUDE = os.path.join(_ROOT, "include")
 HEADER = os.path.join(INCLUDE, "spec_verify.h")
@@ -53,6 +55,7 @@ EXPORTED = (
     "spec_verify_tree",
     "spec_verify_last_error",
     "spec_verify_intermediates",
+    "spec_verify_acceptance",
     "spec_verify_status_string",
 )
 
@@ -113,6 +116,7 @@ def lib():
         L.spec_verify_tree.argtypes = [P, P, P, I, I, I, I, I, P, P, P, P, Z, P]
         L.spec_verify_last_error.argtypes = [P, Z, P]
         L.spec_verify_intermediates.argtypes = [P, Z, I, I, I, P, P, P, P, P]
+        L.spec_verify_acceptance.argtypes = [P, P, I, I, I, F, F, I, P, P, P, Z, P]
         L.spec_verify_status_string.argtypes = [I]
         L.spec_verify_status_string.restype = ctypes.c_char_p
         for name in EXPORTED[:-1]:
@@ -199,6 +203,13 @@ def spec_verify_intermediates(workspace_ptr, workspace_bytes, B, k, V, P_ptr, Q_
                               S_ptr, stream=0):
     return _check(lib().spec_verify_intermediates(workspace_ptr, workspace_bytes, B, k, V,
                                                   P_ptr, Q_ptr, Z_ptr, S_ptr, stream))
+
+
+def spec_verify_acceptance(target_ptr, draft_ptr, B, k, V, temperature, top_p, dtype,
+                           out_beta_ptr, out_tv_ptr, workspace_ptr, workspace_bytes, stream=0):
+    return _check(lib().spec_verify_acceptance(
+        target_ptr, draft_ptr, B, k, V, float(temperature), float(top_p), dtype, out_beta_ptr,
+        out_tv_ptr, workspace_ptr, workspace_bytes, stream))
 
 
 def spec_verify_status_string(status):
@@ -315,3 +326,24 @@ def intermediates(workspace, B, k, V, stream=None):
     spec_verify_intermediates(_ptr(workspace), workspace.numel(), B, k, V, _ptr(P), _ptr(Q),
                               _ptr(Z), _ptr(S), _stream(stream))
     return P, Q, Z, S
+
+
+def acceptance(target, draft, workspace, temperature=1.0, top_p=1.0, out_beta=None, out_tv=None,
+               stream=None):
+    """Tensor-level spec_verify_acceptance: (beta [B, k], tv [B, k]) of the
+    last stochastic verify call made on `workspace` with these arguments."""
+    torch = _torch()
+    B, k1, V = target.shape
+    k = k1 - 1
+    dt = _dtype_code(target)
+    _need(target, "target", target.dtype, (B, k + 1, V))
+    _need(draft, "draft", target.dtype, (B, k, V))
+    dev = target.device
+    if out_beta is None:
+        out_beta = torch.empty((B, k), dtype=torch.float32, device=dev)
+    if out_tv is None:
+        out_tv = torch.empty((B, k), dtype=torch.float32, device=dev)
+    spec_verify_acceptance(_ptr(target), _ptr(draft), B, k, V, temperature, top_p, dt,
+                           _ptr(out_beta), _ptr(out_tv), _ptr(workspace), workspace.numel(),
+                           _stream(stream))
+    return out_beta, out_tv

@@ -39,6 +39,8 @@ size_t carve(void *base, int B, int rows_per_seq, int V, Workspace *ws, bool cha
     const size_t trows = chain ? static_cast<size_t>(B) * ((rows_per_seq + 1) / 2) : 0;
     char *nuc_n = take(trows * sizeof(int32_t));
     char *nuc = take(trows * kNucCap * sizeof(uint4));
+    const size_t pairs = chain ? static_cast<size_t>(B) * ((rows_per_seq - 1) / 2) : 0;
+    char *accq = take(chain ? (pairs + 2) * sizeof(uint32_t) : 0);
     if (ws) {
         ws->err = reinterpret_cast<uint32_t *>(err);
         ws->row_ctr = reinterpret_cast<uint32_t *>(row_ctr);
@@ -50,6 +52,7 @@ size_t carve(void *base, int B, int rows_per_seq, int V, Workspace *ws, bool cha
         ws->seqs = reinterpret_cast<SeqRec *>(seqs);
         ws->nuc_n = reinterpret_cast<int32_t *>(nuc_n);
         ws->nuc = reinterpret_cast<uint4 *>(nuc);
+        ws->accq = reinterpret_cast<uint32_t *>(accq);
         ws->pmax = pmax;
     }
     return off;
@@ -305,6 +308,42 @@ SPEC_EXPORT int spec_verify_intermediates(const void *workspace, size_t workspac
     Workspace ws;
     carve(const_cast<void *>(workspace), B, 2 * k + 1, V, &ws, true);
     return launch_intermediates(ws, B, k, P, Q, Z, S, reinterpret_cast<cudaStream_t>(stream));
+}
+
+SPEC_EXPORT int spec_verify_acceptance(const void *target_logits, const void *draft_logits, int B,
+                                       int k, int V, float temperature, float top_p, int dtype,
+                                       float *out_beta, float *out_tv, void *workspace,
+                                       size_t workspace_bytes, spec_stream_t stream) {
+    if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_DTYPE;
+    if (!chain_sizes_ok(B, k, V)) return SPEC_ERR_SHAPE;
+    if (B == 0) return SPEC_OK;
+    if (!target_logits || !draft_logits || !out_beta || !workspace) return SPEC_ERR_NULL;
+    if (!(temperature > 0.0f) || !std::isfinite(temperature) || !(top_p > 0.0f) ||
+        !(top_p <= 1.0f))
+        return SPEC_ERR_PARAM;
+    const size_t esz = dtype == SPEC_F32 ? 4 : 2;
+    if (!aligned(target_logits, esz) || !aligned(draft_logits, esz) || !aligned(out_beta, 4) ||
+        (out_tv && !aligned(out_tv, 4)) || !aligned(workspace, 16))
+        return SPEC_ERR_ALIGN;
+    if (workspace_bytes < carve(nullptr, B, 2 * k + 1, V, nullptr, true)) return SPEC_ERR_WORKSPACE;
+    AcceptArgs a;
+    carve(workspace, B, 2 * k + 1, V, &a.ws, true);
+    a.rows.target = target_logits;
+    a.rows.draft = draft_logits;
+    a.rows.V = V;
+    a.rows.k = k;
+    a.rows.R = 2 * k + 1;
+    a.rows.draft_rows_from = k + 1;
+    a.rows.tgt_rows_per_seq = k + 1;
+    a.pairs = static_cast<long long>(B) * k;
+    a.total = a.pairs * V;
+    a.seg = 0;
+    a.c = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
+    const bool masked = top_p < 1.0f;
+    a.list = masked ? 1 : 0;
+    a.beta = out_beta;
+    a.tv = out_tv;
+    return launch_accept(a, dtype, masked, reinterpret_cast<cudaStream_t>(stream));
 }
 
 SPEC_EXPORT const char *spec_verify_status_string(int status) {

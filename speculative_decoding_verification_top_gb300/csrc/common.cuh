@@ -76,6 +76,7 @@ struct Workspace {
     SeqRec *seqs;          // [B]
     int32_t *nuc_n;        // [B (k+1)] entries of each target row's nucleus list, or -1 (top-p)
     uint4 *nuc;            // [B (k+1), kNucCap] (index, target logit, draft logit at it), index order
+    uint32_t *accq;        // acceptance queue: [0] length, [1] CTA arrivals, then [B k] pair ids
     int pmax;              // partial slots per row
 };
 
@@ -607,6 +608,18 @@ struct FinalArgs {
     Workspace ws;
 };
 
+struct AcceptArgs {
+    RowView rows;      // the verify call's rows (R = 2k+1)
+    long long pairs;   // B k (target row i, draft row i) pairs
+    long long total;   // pairs * V: the pairs end to end
+    long long seg;     // elements per warp segment
+    float c;           // log2(e) / temperature
+    int list;          // top-p: sum over the target rows' nucleus lists where present
+    Workspace ws;
+    float *beta;       // [B, k]
+    float *tv;         // [B, k] or null
+};
+
 struct TreeArgs {
     const int32_t *parents;
     const int32_t *node_tokens;
@@ -649,6 +662,9 @@ int launch_topp_rows(const ToppArgs &a, int rows_total, int dtype, cudaStream_t 
 // The final kernel is launched as a programmatic dependent of the row kernel.
 int launch_final(const FinalArgs &a, int dtype, cudaStream_t st);
 int launch_tree(const TreeArgs &a, cudaStream_t st);
+// Acceptance rate per (sequence, position) from a verify call's row records;
+// masked: the rows carry nucleus keys (top-p).
+int launch_accept(const AcceptArgs &a, int dtype, bool masked, cudaStream_t st);
 int launch_intermediates(const Workspace &ws, int B, int k, float *P, float *Q, float *Z,
                          float *S, cudaStream_t st);
 
