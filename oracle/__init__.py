@@ -32,12 +32,14 @@ ROW_ALL_NEG_INF = 2
 TOKEN_RANGE = 3
 UNIFORM_RANGE = 4
 TREE_SHAPE = 5
+PROB_RANGE = 6
 CODE_NAMES = {
     ROW_NONFINITE: "ROW_NONFINITE",
     ROW_ALL_NEG_INF: "ROW_ALL_NEG_INF",
     TOKEN_RANGE: "TOKEN_RANGE",
     UNIFORM_RANGE: "UNIFORM_RANGE",
     TREE_SHAPE: "TREE_SHAPE",
+    PROB_RANGE: "PROB_RANGE",
 }
 
 _lib = None
@@ -69,6 +71,8 @@ def _load():
         lib.oracle_inverse_cdf.restype = ctypes.c_int32
         lib.oracle_verify_sample.argtypes = [P, P, I, P, P, I, I, I, D, D, I, P, P, P, P]
         lib.oracle_verify_sample.restype = I
+        lib.oracle_verify_sample_probs.argtypes = [P, P, I, P, P, I, I, I, D, D, P, P, P, P]
+        lib.oracle_verify_sample_probs.restype = I
         lib.oracle_acceptance.argtypes = [P, P, I, I, I, I, D, D, P, P]
         lib.oracle_acceptance.restype = I
         lib.oracle_ancestor_mask.argtypes = [P, I, P]
@@ -151,6 +155,35 @@ def verify_sample(target, draft, draft_tokens, uniforms, T=1.0, top_p=1.0, mode=
         _ptr(out_t), _ptr(out_n), _ptr(dbg), _ptr(info))
     if err < 0:
         raise ValueError("oracle_verify_sample rejected its arguments")
+    res = dict(tokens=out_t, num_accepted=out_n, errors=err)
+    if debug:
+        res.update(dbg=dbg, row_info=info)
+    return res
+
+
+def verify_sample_probs(target, draft_probs, draft_tokens, uniforms, T=1.0, top_p=1.0,
+                        debug=False):
+    """verify_sample with the draft given as probabilities: draft_probs
+    [B, k, V] float32 is q itself (used as given; temperature and top-p
+    process the target rows only).  Same results; with debug=True row_info
+    is [B, k+1, 4] (target rows)."""
+    tgt, dt = _logits(target)
+    B, k1, V = tgt.shape
+    k = k1 - 1
+    q = np.ascontiguousarray(draft_probs, np.float32)
+    if q.shape != (B, k, V):
+        raise ValueError("draft_probs must be float32 [B, k, V]")
+    toks = np.ascontiguousarray(draft_tokens, np.int32).reshape(B, k)
+    uni = np.ascontiguousarray(uniforms, np.float32).reshape(B, k + 1)
+    out_t = np.zeros((B, k + 1), np.int32)
+    out_n = np.zeros(B, np.int32)
+    dbg = np.zeros((B, 2 * k + 3), np.float64) if debug else None
+    info = np.zeros((B, k + 1, 4), np.float64) if debug else None
+    err = _load().oracle_verify_sample_probs(
+        _ptr(tgt), _ptr(q), dt, _ptr(toks), _ptr(uni), B, k, V, float(T), float(top_p),
+        _ptr(out_t), _ptr(out_n), _ptr(dbg), _ptr(info))
+    if err < 0:
+        raise ValueError("oracle_verify_sample_probs rejected its arguments")
     res = dict(tokens=out_t, num_accepted=out_n, errors=err)
     if debug:
         res.update(dbg=dbg, row_info=info)

@@ -46,6 +46,12 @@
  *   R7 data errors: a row holding NaN or +inf, a row that is entirely -inf,
  *      a token outside [0, V) or a uniform outside [0, 1) marks the whole
  *      sequence as failed: its tokens and its accepted count are -1.
+ *   R8 draft given as probabilities: the step takes the draft "logits (or
+ *      probabilities)".  Reading: a probability row is q itself, the
+ *      distribution the drafter sampled from -- used as given (no
+ *      temperature, no top-p, no renormalisation); only p is processed.
+ *      The k gathered values q_i(x~_i) must lie in [0, 1] (R7 otherwise);
+ *      the rest of a row is not checked.
  */
 #include <math.h>
 #include <stdint.h>
@@ -63,8 +69,9 @@ enum {
     ORC_ROW_ALL_NEG_INF = 2, /* every logit of the row is -inf            */
     ORC_TOKEN_RANGE = 3,     /* a draft or node token outside [0, V)      */
     ORC_UNIFORM_RANGE = 4,   /* a uniform outside [0, 1)                  */
-    ORC_TREE_SHAPE = 5       /* parents not a rooted tree in topological
+    ORC_TREE_SHAPE = 5,      /* parents not a rooted tree in topological
                                 order, or a node deeper than D            */
+    ORC_PROB_RANGE = 6       /* a gathered draft probability not in [0, 1] */
 };
 
 /* ---------------------------------------------------------------- input */
@@ -254,6 +261,55 @@ static void fail_sequence(int32_t *tok, int width, int32_t *num)
 }
 
 /*
+ * The accept scan and the final draw of one sequence whose rows passed
+ * every check.  p: the k+1 processed target rows, q: the k draft rows (V
+ * doubles each, row-major); xt: the k draft tokens; ub: the k+1 uniforms;
+ * w: V doubles of scratch.  Writes the sequence's tokens and j, and (d not
+ * NULL) P_1..P_k, Q_1..Q_k, S, C(token-1), C(token).
+ */
+static void step_sequence(const double *p, const double *q, const int32_t *xt,
+                          const float *ub, int k, int V, double *w, double *d,
+                          int32_t *ot, int32_t *num)
+{
+    /* Accept x~_i iff u_i * q_i(x~_i) < p_i(x~_i) (R2), left to right,
+     * stopping at the first rejection. */
+    int j = k;
+    for (int i = 0; i < k; ++i) {
+        double P = p[(size_t)i * V + xt[i]];
+        double Q = q[(size_t)i * V + xt[i]];
+        if (d) {
+            d[i] = P;
+            d[k + i] = Q;
+        }
+        if (j == k && !((double)ub[i] * Q < P)) j = i;
+    }
+
+    /* Residual max(0, p - q) at the rejecting position ([LZ] step 3,
+     * [MN] 2.2, [LB] step 3), or p_{k+1} when all k were accepted
+     * ([LZ] step 4 "Bonus token"). */
+    const double *p_row = p + (size_t)j * V;
+    if (j < k) {
+        const double *q_row = q + (size_t)j * V;
+        double S = 0.0;
+        for (int x = 0; x < V; ++x) {
+            double diff = p_row[x] - q_row[x];
+            w[x] = diff > 0.0 ? diff : 0.0;
+            S += w[x];
+        }
+        if (!(S > 0.0)) /* R4 */
+            memcpy(w, p_row, (size_t)V * sizeof *w);
+    } else {
+        memcpy(w, p_row, (size_t)V * sizeof *w);
+    }
+    int32_t drawn = oracle_inverse_cdf(w, V, (double)ub[k], d ? d + 2 * k : NULL);
+
+    for (int i = 0; i < j; ++i) ot[i] = xt[i];
+    ot[j] = drawn;
+    for (int i = j + 1; i <= k; ++i) ot[i] = -1;
+    *num = j;
+}
+
+/*
  * One verification step for B independent sequences ([LZ] "The algorithm
  * (one step)"; [MN] 3.3; [LB] "The Modified Rejection Sampling Algorithm").
  *
@@ -345,48 +401,71 @@ int oracle_verify_sample(const void *target, const void *draft, int dtype,
             continue;
         }
 
-        /* Accept x~_i iff u_i * q_i(x~_i) < p_i(x~_i) (R2), left to right,
-         * stopping at the first rejection. */
-        double *d = dbg ? dbg + (size_t)b * (2 * k + 3) : NULL;
-        int j = k;
-        for (int i = 0; i < k; ++i) {
-            double P = prob[(size_t)i * V + xt[i]];
-            double Q = prob[(size_t)(k + 1 + i) * V + xt[i]];
-            if (d) {
-                d[i] = P;
-                d[k + i] = Q;
-            }
-            if (j == k && !((double)ub[i] * Q < P)) j = i;
-        }
-
-        /* Residual max(0, p - q) at the rejecting position ([LZ] step 3,
-         * [MN] 2.2, [LB] step 3), or p_{k+1} when all k were accepted
-         * ([LZ] step 4 "Bonus token"). */
-        const double *p_row = prob + (size_t)j * V;
-        if (j < k) {
-            const double *q_row = prob + (size_t)(k + 1 + j) * V;
-            double S = 0.0;
-            for (int x = 0; x < V; ++x) {
-                double diff = p_row[x] - q_row[x];
-                w[x] = diff > 0.0 ? diff : 0.0;
-                S += w[x];
-            }
-            if (!(S > 0.0)) /* R4 */
-                memcpy(w, p_row, (size_t)V * sizeof *w);
-        } else {
-            memcpy(w, p_row, (size_t)V * sizeof *w);
-        }
-        int32_t drawn = oracle_inverse_cdf(w, V, (double)ub[k],
-                                           d ? d + 2 * k : NULL);
-
-        for (int i = 0; i < j; ++i) ot[i] = xt[i];
-        ot[j] = drawn;
-        for (int i = j + 1; i <= k; ++i) ot[i] = -1;
-        out_num[b] = j;
+        step_sequence(prob, prob + (size_t)(k + 1) * V, xt, ub, k, V, w,
+                      dbg ? dbg + (size_t)b * (2 * k + 3) : NULL, ot, &out_num[b]);
     }
     free(prob);
     free(w);
     free(g);
+    return errors;
+}
+
+/*
+ * oracle_verify_sample (STOCHASTIC) with the draft given as probabilities
+ * (R8): draft_probs [B, k, V] fp32 is q_1..q_k as given; the target rows
+ * are processed as usual.  Same outputs; row_info [B, k+1, 4] (optional)
+ * covers the target rows only.
+ */
+int oracle_verify_sample_probs(const void *target, const float *draft_probs,
+                               int dtype, const int32_t *tokens,
+                               const float *uniforms, int B, int k, int V,
+                               double T, double top_p, int32_t *out_tokens,
+                               int32_t *out_num, double *dbg, double *row_info)
+{
+    if (!target || !draft_probs || !tokens || !uniforms || !out_tokens ||
+        !out_num || B < 0 || k < 1 || V < 1 ||
+        (dtype != ORC_F32 && dtype != ORC_BF16) || !(T > 0.0) ||
+        !(top_p > 0.0) || top_p > 1.0)
+        return ORC_BAD_ARGUMENT;
+    const size_t esz = dtype == ORC_F32 ? 4 : 2;
+    double *p = (double *)malloc((size_t)(k + 1) * V * sizeof *p);
+    double *q = (double *)malloc((size_t)k * V * sizeof *q);
+    double *w = (double *)malloc((size_t)V * sizeof *w);
+    int errors = 0;
+    for (int b = 0; b < B; ++b) {
+        int32_t *ot = out_tokens + (size_t)b * (k + 1);
+        const int32_t *xt = tokens + (size_t)b * k;
+        const float *ub = uniforms + (size_t)b * (k + 1);
+        const float *qb = draft_probs + (size_t)b * k * V;
+        int bad = 0;
+        for (int i = 0; i < k; ++i) {
+            if (xt[i] < 0 || xt[i] >= V) {
+                bad |= 1 << ORC_TOKEN_RANGE;
+                continue;
+            }
+            float g = qb[(size_t)i * V + xt[i]];
+            if (!(g >= 0.0f && g <= 1.0f)) bad |= 1 << ORC_PROB_RANGE;
+        }
+        for (int i = 0; i <= k; ++i)
+            if (!(ub[i] >= 0.0f && ub[i] < 1.0f)) bad |= 1 << ORC_UNIFORM_RANGE;
+        for (int r = 0; r <= k; ++r) {
+            const char *row = (const char *)target + ((size_t)b * (k + 1) + r) * V * esz;
+            double *info = row_info ? row_info + ((size_t)b * (k + 1) + r) * 4 : NULL;
+            int status = oracle_process_row(row, dtype, V, T, top_p, p + (size_t)r * V, info);
+            if (status != ORC_OK) bad |= 1 << status;
+        }
+        if (bad) {
+            errors |= bad;
+            fail_sequence(ot, k + 1, &out_num[b]);
+            continue;
+        }
+        for (size_t e = 0; e < (size_t)k * V; ++e) q[e] = (double)qb[e];
+        step_sequence(p, q, xt, ub, k, V, w, dbg ? dbg + (size_t)b * (2 * k + 3) : NULL,
+                      ot, &out_num[b]);
+    }
+    free(p);
+    free(q);
+    free(w);
     return errors;
 }
 
