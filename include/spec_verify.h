@@ -77,9 +77,11 @@ enum {
     SPEC_DATA_TOKEN_RANGE = 1 << 3,     /* a draft or node token not in
                                            [0, V)                          */
     SPEC_DATA_UNIFORM_RANGE = 1 << 4,   /* a uniform not in [0, 1)         */
-    SPEC_DATA_TREE_SHAPE = 1 << 5       /* parents not a rooted tree in
+    SPEC_DATA_TREE_SHAPE = 1 << 5,      /* parents not a rooted tree in
                                            topological order, or a node
                                            deeper than D                   */
+    SPEC_DATA_PROB_RANGE = 1 << 6       /* a gathered draft probability
+                                           q_i(x~_i) not in [0, 1]         */
 };
 
 /* Supported ranges. */
@@ -175,6 +177,35 @@ int spec_verify_sample_finish(const void *target_logits, const void *draft_logit
                               int mode, int dtype, int32_t *out_tokens,
                               int32_t *out_num_accepted, void *workspace,
                               size_t workspace_bytes, spec_stream_t stream);
+
+/*
+ * spec_verify_sample (SPEC_STOCHASTIC) with the draft given as
+ * probabilities instead of logits: the step takes "draft logits (or
+ * probabilities)".  draft_probs [B, k, V] fp32 is q_1..q_k itself -- the
+ * distributions the drafter sampled x~_i from -- and is used as given: no
+ * temperature, no top-p, no renormalisation.  temperature and top_p
+ * process the target rows only (p_i as in spec_verify_sample).  Draft rows
+ * are read only where the step needs them: q_i(x~_i) at each draft token,
+ * and the rejecting position's row for the residual max(0, p - q).
+ *
+ * Arguments as for spec_verify_sample, except
+ *   draft_probs      [B, k, V] fp32, device, 4-byte aligned (any dtype of
+ *                    target_logits)
+ *   dtype            storage type of target_logits
+ * Data errors as for spec_verify_sample, plus SPEC_DATA_PROB_RANGE: a
+ * gathered q_i(x~_i) that is NaN or outside [0, 1] fails the sequence.  The
+ * rest of each row is not checked: it must hold finite, non-negative values
+ * (a NaN there weighs zero in the residual).
+ * spec_verify_intermediates after this call: P, Q and S as documented; Z
+ * holds the k+1 target rows of each sequence only, packed at stride k+1.
+ * spec_verify_acceptance does not apply to this form.
+ */
+int spec_verify_sample_probs(const void *target_logits, const float *draft_probs,
+                             const int32_t *draft_tokens, const float *uniforms,
+                             int B, int k, int V, float temperature, float top_p,
+                             int dtype, int32_t *out_tokens, int32_t *out_num_accepted,
+                             void *workspace, size_t workspace_bytes,
+                             spec_stream_t stream);
 
 /*
  * Greedy tree verification for B sequences sharing one candidate tree --

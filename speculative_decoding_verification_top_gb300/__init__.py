@@ -10,9 +10,9 @@ Entry points (same names as the C ABI):
     spec_verify_workspace_size, spec_verify_tree_workspace_size,
     spec_verify_workspace_init, spec_verify_sample, spec_verify_tree,
     spec_verify_last_error, spec_verify_intermediates,
-    spec_verify_acceptance, spec_verify_status_string
-plus tensor-level helpers ``verify_sample`` / ``verify_tree`` /
-``acceptance`` that take
+    spec_verify_acceptance, spec_verify_sample_probs, spec_verify_status_string
+plus tensor-level helpers ``verify_sample`` / ``verify_sample_probs`` /
+``verify_tree`` / ``acceptance`` that take
 torch CUDA tensors, allocate outputs and a zeroed workspace, and raise on a
 negative status.
 """
@@ -42,6 +42,7 @@ SPEC_DATA_ROW_ALL_NEG_INF = 1 << 2
 SPEC_DATA_TOKEN_RANGE = 1 << 3
 SPEC_DATA_UNIFORM_RANGE = 1 << 4
 SPEC_DATA_TREE_SHAPE = 1 << 5
+SPEC_DATA_PROB_RANGE = 1 << 6
 SPEC_MAX_K = 31
 
 EXPORTED = (
@@ -56,6 +57,7 @@ EXPORTED = (
     "spec_verify_last_error",
     "spec_verify_intermediates",
     "spec_verify_acceptance",
+    "spec_verify_sample_probs",
     "spec_verify_status_string",
 )
 
@@ -117,6 +119,7 @@ def lib():
         L.spec_verify_last_error.argtypes = [P, Z, P]
         L.spec_verify_intermediates.argtypes = [P, Z, I, I, I, P, P, P, P, P]
         L.spec_verify_acceptance.argtypes = [P, P, I, I, I, F, F, I, P, P, P, Z, P]
+        L.spec_verify_sample_probs.argtypes = [P, P, P, P, I, I, I, F, F, I, P, P, P, Z, P]
         L.spec_verify_status_string.argtypes = [I]
         L.spec_verify_status_string.restype = ctypes.c_char_p
         for name in EXPORTED[:-1]:
@@ -212,6 +215,15 @@ def spec_verify_acceptance(target_ptr, draft_ptr, B, k, V, temperature, top_p, d
         out_tv_ptr, workspace_ptr, workspace_bytes, stream))
 
 
+def spec_verify_sample_probs(target_ptr, draft_probs_ptr, tokens_ptr, uniforms_ptr, B, k, V,
+                             temperature, top_p, dtype, out_tokens_ptr, out_num_ptr,
+                             workspace_ptr, workspace_bytes, stream=0):
+    return _check(lib().spec_verify_sample_probs(
+        target_ptr, draft_probs_ptr, tokens_ptr, uniforms_ptr, B, k, V, float(temperature),
+        float(top_p), dtype, out_tokens_ptr, out_num_ptr, workspace_ptr, workspace_bytes,
+        stream))
+
+
 def spec_verify_status_string(status):
     return lib().spec_verify_status_string(int(status)).decode()
 
@@ -281,6 +293,32 @@ def verify_sample(target, draft, draft_tokens, uniforms, temperature=1.0, top_p=
                        _ptr(draft_tokens), _ptr(uniforms) if mode == SPEC_STOCHASTIC else None,
                        B, k, V, temperature, top_p, mode, dt, _ptr(out_tokens), _ptr(out_num),
                        _ptr(workspace), workspace.numel(), _stream(stream))
+    return out_tokens, out_num, workspace
+
+
+def verify_sample_probs(target, draft_probs, draft_tokens, uniforms, temperature=1.0, top_p=1.0,
+                        out_tokens=None, out_num=None, workspace=None, stream=None):
+    """Tensor-level spec_verify_sample_probs (draft given as fp32
+    probabilities [B, k, V]).  Returns (out_tokens, out_num_accepted,
+    workspace)."""
+    torch = _torch()
+    B, k1, V = target.shape
+    k = k1 - 1
+    dt = _dtype_code(target)
+    _need(target, "target", target.dtype, (B, k + 1, V))
+    _need(draft_probs, "draft_probs", torch.float32, (B, k, V))
+    _need(uniforms, "uniforms", torch.float32, (B, k + 1))
+    _need(draft_tokens, "draft_tokens", torch.int32, (B, k))
+    dev = target.device
+    if out_tokens is None:
+        out_tokens = torch.empty((B, k + 1), dtype=torch.int32, device=dev)
+    if out_num is None:
+        out_num = torch.empty((B,), dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = new_workspace(spec_verify_workspace_size(B, k, V), dev)
+    spec_verify_sample_probs(_ptr(target), _ptr(draft_probs), _ptr(draft_tokens), _ptr(uniforms),
+                             B, k, V, temperature, top_p, dt, _ptr(out_tokens), _ptr(out_num),
+                             _ptr(workspace), workspace.numel(), _stream(stream))
     return out_tokens, out_num, workspace
 
 

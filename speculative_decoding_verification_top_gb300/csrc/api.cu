@@ -81,10 +81,13 @@ struct ChainPlan {
     cudaStream_t st;
 };
 
+// qprob: draft_logits holds fp32 probabilities q [B, k, V], used as given
+// (stochastic mode only); the rows streamed are the k+1 target rows.
 int plan_chain(const void *target_logits, const void *draft_logits, const int32_t *draft_tokens,
                const float *uniforms, int B, int k, int V, float temperature, float top_p,
                int mode, int dtype, int32_t *out_tokens, int32_t *out_num_accepted,
-               void *workspace, size_t workspace_bytes, spec_stream_t stream, ChainPlan *plan) {
+               void *workspace, size_t workspace_bytes, spec_stream_t stream, ChainPlan *plan,
+               bool qprob = false) {
     if (mode != SPEC_STOCHASTIC && mode != SPEC_GREEDY) return SPEC_ERR_MODE;
     if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_DTYPE;
     if (!chain_sizes_ok(B, k, V)) return SPEC_ERR_SHAPE;
@@ -97,7 +100,7 @@ int plan_chain(const void *target_logits, const void *draft_logits, const int32_
                   !(top_p <= 1.0f)))
         return SPEC_ERR_PARAM;
     const size_t esz = dtype == SPEC_F32 ? 4 : 2;
-    if (!aligned(target_logits, esz) || (stoch && !aligned(draft_logits, esz)) ||
+    if (!aligned(target_logits, esz) || (stoch && !aligned(draft_logits, qprob ? 4 : esz)) ||
         !aligned(draft_tokens, 4) || (stoch && !aligned(uniforms, 4)) ||
         !aligned(out_tokens, 4) || !aligned(out_num_accepted, 4) || !aligned(workspace, 16))
         return SPEC_ERR_ALIGN;
@@ -117,7 +120,7 @@ int plan_chain(const void *target_logits, const void *draft_logits, const int32_
     rv.draft = draft_logits;
     rv.V = V;
     rv.k = k;
-    rv.R = stoch ? 2 * k + 1 : k + 1;
+    rv.R = stoch && !qprob ? 2 * k + 1 : k + 1;
     rv.draft_rows_from = k + 1;
     rv.tgt_rows_per_seq = k + 1;
     plan->rows_total = B * rv.R;
@@ -125,6 +128,7 @@ int plan_chain(const void *target_logits, const void *draft_logits, const int32_
     FinalArgs &fa = plan->fin;
     fa.target = target_logits;
     fa.draft = draft_logits;
+    fa.qprob = qprob ? 1 : 0;
     fa.draft_tokens = draft_tokens;
     fa.uniforms = uniforms;
     fa.B = B;
@@ -139,6 +143,7 @@ int plan_chain(const void *target_logits, const void *draft_logits, const int32_
     SeqArgs &sq = plan->seq;
     sq.work = stoch ? kSeqDecide : kSeqGreedy;
     sq.list_draw = stoch && top_p < 1.0f ? 1 : 0;
+    sq.qprob = qprob ? 1 : 0;
     sq.draft_tokens = draft_tokens;
     sq.uniforms = uniforms;
     sq.out_tokens = out_tokens;
@@ -235,6 +240,22 @@ SPEC_EXPORT int spec_verify_sample_finish(const void *target_logits, const void 
                               temperature, top_p, mode, dtype, out_tokens, out_num_accepted,
                               workspace, workspace_bytes, stream, &plan);
     if (rc != SPEC_OK || B == 0) return rc;
+    return launch_chain_finish(plan);
+}
+
+SPEC_EXPORT int spec_verify_sample_probs(const void *target_logits, const float *draft_probs,
+                                         const int32_t *draft_tokens, const float *uniforms,
+                                         int B, int k, int V, float temperature, float top_p,
+                                         int dtype, int32_t *out_tokens,
+                                         int32_t *out_num_accepted, void *workspace,
+                                         size_t workspace_bytes, spec_stream_t stream) {
+    ChainPlan plan;
+    int rc = plan_chain(target_logits, draft_probs, draft_tokens, uniforms, B, k, V, temperature,
+                        top_p, SPEC_STOCHASTIC, dtype, out_tokens, out_num_accepted, workspace,
+                        workspace_bytes, stream, &plan, true);
+    if (rc != SPEC_OK || B == 0) return rc;
+    rc = launch_chain_rows(plan);
+    if (rc != SPEC_OK) return rc;
     return launch_chain_finish(plan);
 }
 
@@ -363,6 +384,7 @@ SPEC_EXPORT const char *spec_verify_status_string(int status) {
     case SPEC_DATA_UNIFORM_RANGE: return "a uniform lies outside [0, 1)";
     case SPEC_DATA_TREE_SHAPE:
         return "parents is not a rooted tree in topological order within depth D";
+    case SPEC_DATA_PROB_RANGE: return "a gathered draft probability lies outside [0, 1]";
     default: return "unknown status";
     }
 }

@@ -347,6 +347,7 @@ enum SeqWork { kSeqDecide = 0, kSeqGreedy = 1, kSeqNone = 2 };
 struct SeqArgs {
     int work;                    // SeqWork
     int list_draw;               // draw from the rows' nucleus lists where they exist (top-p)
+    int qprob;                   // the draft rows are fp32 probabilities q, used as given
     const int32_t *draft_tokens; // [B, k]
     const float *uniforms;       // [B, k+1] (kSeqDecide)
     int32_t *out_tokens;         // [B, k+1]
@@ -354,20 +355,21 @@ struct SeqArgs {
 };
 
 // Weight of nucleus entry e of the draw row (index, target logit, draft
-// logit at that index): p(x), or max(0, p(x) - q(x)).
-template <typename T>
+// logit -- or, QP, draft probability -- at that index): p(x), or
+// max(0, p(x) - q(x)).
+template <typename T, bool QP>
 __device__ __forceinline__ float list_weight(uint4 e, float c, bool use_p, float pneg, float pinv,
                                              uint32_t plam, float qneg, float qinv,
                                              uint32_t qlam) {
     const float p = proc_prob<T>(__uint_as_float(e.y), c, pneg, pinv, plam);
     if (use_p) return p;
-    const float q = proc_prob<T>(__uint_as_float(e.z), c, qneg, qinv, qlam);
+    const float q = QP ? __uint_as_float(e.z) : proc_prob<T>(__uint_as_float(e.z), c, qneg, qinv, qlam);
     return fmaxf(__fsub_rn(p, q), 0.0f);
 }
 
 // Total weight over a nucleus list: rounds of 32 entries in index order,
 // each round's total as warp_excl_scan defines it, folded in order.
-template <typename T>
+template <typename T, bool QP>
 __device__ float list_total(const uint4 *L, int n, float c, bool use_p, float pneg, float pinv,
                             uint32_t plam, float qneg, float qinv, uint32_t qlam) {
     const int lane = threadIdx.x & 31;
@@ -375,8 +377,8 @@ __device__ float list_total(const uint4 *L, int n, float c, bool use_p, float pn
 #pragma unroll 4
     for (int r0 = 0; r0 < n; r0 += 32) {
         const int i = r0 + lane;
-        const float w = i < n ? list_weight<T>(__ldcg(L + i), c, use_p, pneg, pinv, plam, qneg,
-                                               qinv, qlam)
+        const float w = i < n ? list_weight<T, QP>(__ldcg(L + i), c, use_p, pneg, pinv, plam,
+                                                   qneg, qinv, qlam)
                               : 0.0f;
         float rt;
         warp_excl_scan(w, rt);
@@ -392,25 +394,25 @@ __device__ float list_total(const uint4 *L, int n, float c, bool use_p, float pn
 // the first entry with w > 0 whose cumulative weight exceeds u S (else the
 // last with w > 0); an empty residual draws from p instead.  Returns false
 // (nothing written) if the row has no list.
-template <typename T>
+template <typename T, bool QP>
 __device__ bool list_draw(const RowView &v, const SeqArgs &sa, const Workspace &ws, float c,
                           int b, int j, SeqRec *rec) {
-    const int lane = threadIdx.x & 31, k = v.k, R = 2 * k + 1;
+    const int lane = threadIdx.x & 31, k = v.k, R = v.R;
     const int tr = b * (k + 1) + j;  // the draw's target row among the target rows
     const int n = __ldcg(&ws.nuc_n[tr]);
     if (n < 0) return false;
     const RowRec *rr = ws.rows + static_cast<size_t>(b) * R;
     const RowRec *pr = rr + j;
-    const RowRec *qr = j < k ? rr + k + 1 + j : pr;
+    const RowRec *qr = !QP && j < k ? rr + k + 1 + j : pr;
     const float pneg = -__fmul_rn(__ldcg(&pr->m), c), pinv = __frcp_rn(__ldcg(&pr->z));
     const float qneg = -__fmul_rn(__ldcg(&qr->m), c), qinv = __frcp_rn(__ldcg(&qr->z));
     const uint32_t plam = __ldcg(&pr->lam_key), qlam = __ldcg(&qr->lam_key);
     const uint4 *L = ws.nuc + static_cast<size_t>(tr) * kNucCap;
     bool use_p = j == k;
-    float S = list_total<T>(L, n, c, use_p, pneg, pinv, plam, qneg, qinv, qlam);
+    float S = list_total<T, QP>(L, n, c, use_p, pneg, pinv, plam, qneg, qinv, qlam);
     if (!(S > 0.0f) && !use_p) {
         use_p = true;
-        S = list_total<T>(L, n, c, use_p, pneg, pinv, plam, qneg, qinv, qlam);
+        S = list_total<T, QP>(L, n, c, use_p, pneg, pinv, plam, qneg, qinv, qlam);
     }
     const float target = __fmul_rn(sa.uniforms[static_cast<size_t>(b) * (k + 1) + k], S);
     float Rsum = 0.0f;
@@ -421,7 +423,7 @@ __device__ bool list_draw(const RowView &v, const SeqArgs &sa, const Workspace &
         float w = 0.0f;
         if (i < n) {
             e = __ldcg(L + i);
-            w = list_weight<T>(e, c, use_p, pneg, pinv, plam, qneg, qinv, qlam);
+            w = list_weight<T, QP>(e, c, use_p, pneg, pinv, plam, qneg, qinv, qlam);
         }
         float rt;
         const float excl = warp_excl_scan(w, rt);
@@ -454,13 +456,16 @@ __device__ bool list_draw(const RowView &v, const SeqArgs &sa, const Workspace &
 // rejection).  Lane i tests draft i; ballot + ffs give the first rejection.
 // Row records are read through L2 (they were written by other warps).
 // Writes the sequence record; a sequence with a data error gets -1 outputs.
-template <typename T>
+// QP: the draft rows are probabilities (q_i(x~_i) is read, not computed,
+// and must lie in [0, 1]); the sequence's rows are its k+1 target rows.
+template <typename T, bool QP>
 __device__ void decide_sequence(const RowView &v, const SeqArgs &sa, const Workspace &ws,
                                 float c, int b) {
-    const int lane = threadIdx.x & 31, k = v.k, V = v.V, R = 2 * k + 1;
+    const int lane = threadIdx.x & 31, k = v.k, V = v.V, R = v.R;
     const RowRec *rr = ws.rows + static_cast<size_t>(b) * R;
     const T *tgt = static_cast<const T *>(v.target) + static_cast<size_t>(b) * (k + 1) * V;
     const T *drf = static_cast<const T *>(v.draft) + static_cast<size_t>(b) * k * V;
+    const float *qpb = static_cast<const float *>(v.draft) + static_cast<size_t>(b) * k * V;
     const float *ub = sa.uniforms + static_cast<size_t>(b) * (k + 1);
     uint32_t bad = 0;
     for (int r = lane; r < R; r += 32) bad |= __ldcg(&rr[r].flags);
@@ -471,13 +476,19 @@ __device__ void decide_sequence(const RowView &v, const SeqArgs &sa, const Works
         if (x < 0 || x >= V) {
             bad |= SPEC_DATA_TOKEN_RANGE;
         } else {
-            const RowRec *tp = rr + lane, *dq = rr + k + 1 + lane;
+            const RowRec *tp = rr + lane;
             P = proc_prob<T>(to_f32(tgt[static_cast<size_t>(lane) * V + x]), c,
                              -__fmul_rn(__ldcg(&tp->m), c), __frcp_rn(__ldcg(&tp->z)),
                              __ldcg(&tp->lam_key));
-            Q = proc_prob<T>(to_f32(drf[static_cast<size_t>(lane) * V + x]), c,
-                             -__fmul_rn(__ldcg(&dq->m), c), __frcp_rn(__ldcg(&dq->z)),
-                             __ldcg(&dq->lam_key));
+            if (QP) {
+                Q = qpb[static_cast<size_t>(lane) * V + x];
+                if (!(Q >= 0.0f && Q <= 1.0f)) bad |= SPEC_DATA_PROB_RANGE;
+            } else {
+                const RowRec *dq = rr + k + 1 + lane;
+                Q = proc_prob<T>(to_f32(drf[static_cast<size_t>(lane) * V + x]), c,
+                                 -__fmul_rn(__ldcg(&dq->m), c), __frcp_rn(__ldcg(&dq->z)),
+                                 __ldcg(&dq->lam_key));
+            }
             accept = __fmul_rn(ub[lane], Q) < P;
         }
     }
@@ -498,7 +509,7 @@ __device__ void decide_sequence(const RowView &v, const SeqArgs &sa, const Works
         // The final draw's rows: target row j and draft row j (residual), or
         // the bonus target row k.
         const RowRec *pr = rr + j;
-        const RowRec *qr = j < k ? rr + k + 1 + j : pr;
+        const RowRec *qr = !QP && j < k ? rr + k + 1 + j : pr;
         rec->j = j;
         rec->bad = bad;
         rec->S = 0.0f;
@@ -519,7 +530,7 @@ __device__ void decide_sequence(const RowView &v, const SeqArgs &sa, const Works
         }
     } else if (sa.list_draw) {
         __syncwarp();
-        list_draw<T>(v, sa, ws, c, b, j, rec);
+        list_draw<T, QP>(v, sa, ws, c, b, j, rec);
     }
 }
 
@@ -572,7 +583,10 @@ __device__ __forceinline__ void row_done(const RowView &v, const SeqArgs &sa,
     __syncwarp();
     if (!last) return;
     if (lane == 0) ws.seq_rows[b] = 0u;
-    if (sa.work == kSeqDecide) decide_sequence<T>(v, sa, ws, c, b);
+    if (sa.work == kSeqDecide) {
+        if (sa.qprob) decide_sequence<T, true>(v, sa, ws, c, b);
+        else decide_sequence<T, false>(v, sa, ws, c, b);
+    }
     else greedy_sequence(v, sa, ws, b);
 }
 
@@ -596,7 +610,8 @@ struct ToppArgs {
 
 struct FinalArgs {
     const void *target;
-    const void *draft;
+    const void *draft;     // draft logits (dtype), or fp32 probabilities (qprob)
+    int qprob;
     const int32_t *draft_tokens;
     const float *uniforms;
     int B, k, V;

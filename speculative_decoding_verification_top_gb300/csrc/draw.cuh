@@ -9,10 +9,14 @@
 namespace specv {
 namespace {
 
-// The rows and processing parameters of one sequence's final draw.
-template <typename T>
+// The rows and processing parameters of one sequence's final draw.  QP:
+// the draft row is fp32 probabilities q (qf), used as given.
+template <typename T, bool QP>
 struct Draw {
-    const T *prow, *qrow;
+    const T *prow;
+    const void *qsrc;  // draft row: logits (T), or QP fp32 probabilities
+    __device__ __forceinline__ const T *qrow() const { return static_cast<const T *>(qsrc); }
+    __device__ __forceinline__ const float *qf() const { return static_cast<const float *>(qsrc); }
     float pneg, pinv, qneg, qinv;
     uint32_t plam, qlam;
     bool use_p;  // weights p (bonus row, or empty residual) instead of max(0, p - q)
@@ -21,15 +25,19 @@ struct Draw {
 };
 
 // The draw of sequence b, from the parameters its decider stored.
-template <typename T>
-__device__ __forceinline__ Draw<T> make_draw(const FinalArgs &a, int b, const SeqRec *rec) {
+template <typename T, bool QP>
+__device__ __forceinline__ Draw<T, QP> make_draw(const FinalArgs &a, int b, const SeqRec *rec) {
     const int k = a.k, V = a.V;
     const int j = __ldcg(&rec->j);
-    Draw<T> d;
+    Draw<T, QP> d;
     d.use_p = __ldcg(&rec->use_p) != 0;
     d.prow = static_cast<const T *>(a.target) + (static_cast<size_t>(b) * (k + 1) + j) * V;
-    d.qrow = d.use_p ? d.prow
-                     : static_cast<const T *>(a.draft) + (static_cast<size_t>(b) * k + j) * V;
+    if (d.use_p)
+        d.qsrc = d.prow;
+    else if (QP)
+        d.qsrc = static_cast<const float *>(a.draft) + (static_cast<size_t>(b) * k + j) * V;
+    else
+        d.qsrc = static_cast<const T *>(a.draft) + (static_cast<size_t>(b) * k + j) * V;
     d.pneg = __ldcg(&rec->pneg);
     d.pinv = __ldcg(&rec->pinv);
     d.plam = __ldcg(&rec->plam);
@@ -37,7 +45,7 @@ __device__ __forceinline__ Draw<T> make_draw(const FinalArgs &a, int b, const Se
     d.qinv = __ldcg(&rec->qinv);
     d.qlam = __ldcg(&rec->qlam);
     d.vec = (reinterpret_cast<uintptr_t>(d.prow) & 15u) == 0 &&
-            (reinterpret_cast<uintptr_t>(d.qrow) & 15u) == 0;
+            (reinterpret_cast<uintptr_t>(d.qsrc) & 15u) == 0;
     d.masked = d.plam != 0u || d.qlam != 0u;
     return d;
 }
@@ -74,9 +82,57 @@ __device__ __forceinline__ void load_run(const T *row, int x, int V, bool vec,
     unpack<T>(load_raw<T>(row, x, V, vec), f);
 }
 
-// Draw weights of the VE elements starting at x from their loaded logits.
-template <typename T>
-__device__ __forceinline__ void weights_from(const Draw<T> &d, int x, int V, float c,
+// The draft side of a run of VE elements at x, raw: one 16-byte vector of
+// logits, or (QP) VE fp32 probabilities in VE / 4 vectors; elements at or
+// beyond V read as -inf logits / zero probabilities.
+template <typename T, bool QP>
+struct QRaw {
+    static constexpr int N = QP ? Elem<T>::kPerVec / 4 : 1;
+    uint4 v[N];
+};
+
+template <typename T, bool QP>
+__device__ __forceinline__ void load_q_raw(const Draw<T, QP> &d, int x, int V, QRaw<T, QP> &r) {
+    constexpr int VE = Elem<T>::kPerVec;
+    if (!QP) {
+        r.v[0] = load_raw<T>(d.qrow(), x, V, d.vec);
+    } else if (d.vec && x + VE <= V) {
+#pragma unroll
+        for (int i = 0; i < QRaw<T, QP>::N; ++i)
+            r.v[i] = __ldg(reinterpret_cast<const uint4 *>(d.qf() + x) + i);
+    } else {
+#pragma unroll
+        for (int i = 0; i < QRaw<T, QP>::N; ++i) {
+            uint32_t e4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int xi = x + 4 * i + e;
+                e4[e] = xi < V ? __float_as_uint(d.qf()[xi]) : 0u;
+            }
+            r.v[i] = make_uint4(e4[0], e4[1], e4[2], e4[3]);
+        }
+    }
+}
+
+template <typename T, bool QP>
+__device__ __forceinline__ void unpack_q(const QRaw<T, QP> &r, float (&f)[Elem<T>::kPerVec]) {
+    if (!QP) {
+        unpack<T>(r.v[0], f);
+        return;
+    }
+#pragma unroll
+    for (int i = 0; i < QRaw<T, QP>::N; ++i) {
+        f[4 * i] = __uint_as_float(r.v[i].x);
+        f[4 * i + 1] = __uint_as_float(r.v[i].y);
+        f[4 * i + 2] = __uint_as_float(r.v[i].z);
+        f[4 * i + 3] = __uint_as_float(r.v[i].w);
+    }
+}
+
+// Draw weights of the VE elements starting at x from their loaded target
+// logits lp and draft values lq (logits, or QP probabilities).
+template <typename T, bool QP>
+__device__ __forceinline__ void weights_from(const Draw<T, QP> &d, int x, int V, float c,
                                              const float (&lp)[Elem<T>::kPerVec],
                                              const float (&lq)[Elem<T>::kPerVec],
                                              float (&w)[Elem<T>::kPerVec]) {
@@ -91,7 +147,7 @@ __device__ __forceinline__ void weights_from(const Draw<T> &d, int x, int V, flo
             if (d.use_p) {
                 wv = __fmul_rn(ep, d.pinv);
             } else {
-                const float q = __fmul_rn(ex2(__fmaf_rn(lq[e], c, d.qneg)), d.qinv);
+                const float q = QP ? lq[e] : __fmul_rn(ex2(__fmaf_rn(lq[e], c, d.qneg)), d.qinv);
                 wv = fmaxf(__fmaf_rn(ep, d.pinv, -q), 0.0f);
             }
             w[e] = x + e < V ? wv : 0.0f;
@@ -103,23 +159,13 @@ __device__ __forceinline__ void weights_from(const Draw<T> &d, int x, int V, flo
         const float p = proc_prob<T>(lp[e], c, d.pneg, d.pinv, d.plam);
         float wv = p;
         if (!d.use_p) {
-            const float q = proc_prob<T>(lq[e], c, d.qneg, d.qinv, d.qlam);
+            const float q = QP ? lq[e] : proc_prob<T>(lq[e], c, d.qneg, d.qinv, d.qlam);
             wv = fmaxf(__fsub_rn(p, q), 0.0f);
         }
         w[e] = x + e < V ? wv : 0.0f;
     }
 }
 
-// Draw weights of the VE elements starting at x.
-template <typename T>
-__device__ __forceinline__ void weights(const Draw<T> &d, int x, int V, float c,
-                                        float (&w)[Elem<T>::kPerVec]) {
-    constexpr int VE = Elem<T>::kPerVec;
-    float lp[VE], lq[VE];
-    load_run<T>(d.prow, x, V, d.vec, lp);
-    if (!d.use_p) load_run<T>(d.qrow, x, V, d.vec, lq);
-    weights_from<T>(d, x, V, c, lp, lq, w);
-}
 
 // Element order inside a 1024-element sub-tile: round u, then lane, then the
 // VE elements of the lane's vector -- exactly index order.
@@ -129,36 +175,39 @@ __device__ __forceinline__ int sub_x(int t, int u, int lane) {
 }
 
 // The raw vectors of sub-tile t of both draw rows (this lane's share).
-template <typename T>
+template <typename T, bool QP>
 struct SubLoad {
     static constexpr int ROUNDS = kSubW / (32 * Elem<T>::kPerVec);
-    uint4 p[ROUNDS], q[ROUNDS];
+    uint4 p[ROUNDS];
+    QRaw<T, QP> q[ROUNDS];
 };
 
-template <typename T>
-__device__ __forceinline__ void subtile_load(const Draw<T> &d, int t, int V, SubLoad<T> &L) {
+template <typename T, bool QP>
+__device__ __forceinline__ void subtile_load(const Draw<T, QP> &d, int t, int V,
+                                             SubLoad<T, QP> &L) {
     const int lane = threadIdx.x & 31;
 #pragma unroll
-    for (int u = 0; u < SubLoad<T>::ROUNDS; ++u) {
+    for (int u = 0; u < SubLoad<T, QP>::ROUNDS; ++u) {
         L.p[u] = load_raw<T>(d.prow, sub_x<T>(t, u, lane), V, d.vec);
-        L.q[u] = d.use_p ? L.p[u] : load_raw<T>(d.qrow, sub_x<T>(t, u, lane), V, d.vec);
+        if (!QP) L.q[u].v[0] = d.use_p ? L.p[u] : load_raw<T>(d.qrow(), sub_x<T>(t, u, lane), V, d.vec);
+        else if (!d.use_p) load_q_raw<T, QP>(d, sub_x<T>(t, u, lane), V, L.q[u]);
     }
 }
 
 // Total draw weight of sub-tile t from its loaded vectors: rounds folded
 // in order.
-template <typename T>
-__device__ __forceinline__ float subtile_reduce(const Draw<T> &d, int t, int V, float c,
-                                                const SubLoad<T> &L) {
+template <typename T, bool QP>
+__device__ __forceinline__ float subtile_reduce(const Draw<T, QP> &d, int t, int V, float c,
+                                                const SubLoad<T, QP> &L) {
     constexpr int VE = Elem<T>::kPerVec;
     const int lane = threadIdx.x & 31;
     float total = 0.0f;
 #pragma unroll
-    for (int u = 0; u < SubLoad<T>::ROUNDS; ++u) {
+    for (int u = 0; u < SubLoad<T, QP>::ROUNDS; ++u) {
         float lp[VE], lq[VE], w[VE];
         unpack<T>(L.p[u], lp);
-        unpack<T>(L.q[u], lq);
-        weights_from<T>(d, sub_x<T>(t, u, lane), V, c, lp, lq, w);
+        unpack_q<T, QP>(L.q[u], lq);
+        weights_from<T, QP>(d, sub_x<T>(t, u, lane), V, c, lp, lq, w);
         float v = 0.0f;
 #pragma unroll
         for (int e = 0; e < VE; ++e) v = __fadd_rn(v, w[e]);
@@ -170,26 +219,29 @@ __device__ __forceinline__ float subtile_reduce(const Draw<T> &d, int t, int V, 
 }
 
 // Total draw weight of sub-tile t (all loads issued before any arithmetic).
-template <typename T>
-__device__ float subtile_total(const Draw<T> &d, int t, int V, float c) {
-    SubLoad<T> L;
-    subtile_load<T>(d, t, V, L);
-    return subtile_reduce<T>(d, t, V, c, L);
+template <typename T, bool QP>
+__device__ float subtile_total(const Draw<T, QP> &d, int t, int V, float c) {
+    SubLoad<T, QP> L;
+    subtile_load<T, QP>(d, t, V, L);
+    return subtile_reduce<T, QP>(d, t, V, c, L);
 }
 
 // The smallest x of sub-tile t with w(x) > 0 and pre + C_t(x) > target,
 // where C_t is the in-sub-tile cumulative weight computed with the same
 // association as subtile_total; else the last x with w(x) > 0.  All loads
 // are issued first.
-template <typename T>
-__device__ int subtile_find(const Draw<T> &d, int t, int V, float c, float pre, float target) {
+template <typename T, bool QP>
+__device__ int subtile_find(const Draw<T, QP> &d, int t, int V, float c, float pre,
+                            float target) {
     constexpr int VE = Elem<T>::kPerVec, ROUNDS = kSubW / (32 * VE);
     const int lane = threadIdx.x & 31;
-    uint4 rp[ROUNDS], rq[ROUNDS];
+    uint4 rp[ROUNDS];
+    QRaw<T, QP> rq[ROUNDS];
 #pragma unroll
     for (int u = 0; u < ROUNDS; ++u) {
         rp[u] = load_raw<T>(d.prow, sub_x<T>(t, u, lane), V, d.vec);
-        rq[u] = d.use_p ? rp[u] : load_raw<T>(d.qrow, sub_x<T>(t, u, lane), V, d.vec);
+        if (!QP) rq[u].v[0] = d.use_p ? rp[u] : load_raw<T>(d.qrow(), sub_x<T>(t, u, lane), V, d.vec);
+        else if (!d.use_p) load_q_raw<T, QP>(d, sub_x<T>(t, u, lane), V, rq[u]);
     }
     float R = 0.0f;
     int lastpos = -1, token = -1;
@@ -198,8 +250,8 @@ __device__ int subtile_find(const Draw<T> &d, int t, int V, float c, float pre, 
         const int x0 = sub_x<T>(t, u, lane);
         float lp[VE], lq[VE], w[VE];
         unpack<T>(rp[u], lp);
-        unpack<T>(rq[u], lq);
-        weights_from<T>(d, x0, V, c, lp, lq, w);
+        unpack_q<T, QP>(rq[u], lq);
+        weights_from<T, QP>(d, x0, V, c, lp, lq, w);
         float v = 0.0f;
 #pragma unroll
         for (int e = 0; e < VE; ++e) v = __fadd_rn(v, w[e]);
@@ -317,29 +369,29 @@ __device__ inline Pick pick_subtile(const float *sums, int NS, float u) {
 // for the token and emit the sequence's outputs (a sequence with a data
 // error already has its -1 outputs).  Leaves the sequence's counter at
 // zero for the next call.
-template <typename T>
+template <typename T, bool QP>
 __device__ void finish_sequence(const FinalArgs &a, int b) {
     const int lane = threadIdx.x & 31, k = a.k, V = a.V;
     SeqRec *rec = a.ws.seqs + b;
     if (lane == 0) a.ws.seq_ctr[b] = 0u;
     if (__ldcg(&rec->bad) || __ldcg(&rec->done)) return;  // outputs already written
-    Draw<T> d = make_draw<T>(a, b, rec);
+    Draw<T, QP> d = make_draw<T, QP>(a, b, rec);
     float *sums = a.ws.sub_sums + static_cast<size_t>(b) * a.NS;
     const float u = a.uniforms[static_cast<size_t>(b) * (k + 1) + k];
     Pick pk = pick_subtile(sums, a.NS, u);
     if (!(pk.S > 0.0f) && !d.use_p) {
         // The residual is zero everywhere: draw from p_{j+1} instead.
         d.use_p = true;
-        d.qrow = d.prow;
+        d.qsrc = d.prow;
         for (int s = 0; s < a.NS; ++s) {
-            const float st = subtile_total<T>(d, s, V, a.c);
+            const float st = subtile_total<T, QP>(d, s, V, a.c);
             if (lane == 0) sums[s] = st;
         }
         __threadfence();
         __syncwarp();
         pk = pick_subtile(sums, a.NS, u);
     }
-    const int tok = subtile_find<T>(d, pk.t, V, a.c, pk.pre, pk.target);
+    const int tok = subtile_find<T, QP>(d, pk.t, V, a.c, pk.pre, pk.target);
     const int j = __ldcg(&rec->j);
     int32_t *ot = a.out_tokens + static_cast<size_t>(b) * (k + 1);
     if (lane <= k) {
@@ -357,15 +409,15 @@ __device__ void finish_sequence(const FinalArgs &a, int b) {
 // Sum sub-tiles [t0, t1) of sequence b's draw into its sub-tile sums and
 // report them; the last report finishes the sequence.  A sequence with a
 // data error, or already drawn, reports without summing.
-template <typename T>
+template <typename T, bool QP>
 __device__ __forceinline__ void draw_run(const FinalArgs &a, int b, int t0, int t1) {
     const int lane = threadIdx.x & 31;
     const SeqRec *rec = a.ws.seqs + b;
     if (!__ldcg(&rec->bad) && !__ldcg(&rec->done)) {
-        const Draw<T> d = make_draw<T>(a, b, rec);
+        const Draw<T, QP> d = make_draw<T, QP>(a, b, rec);
         float *sums = a.ws.sub_sums + static_cast<size_t>(b) * a.NS;
         for (int t = t0; t < t1; ++t) {
-            const float tot = subtile_total<T>(d, t, a.V, a.c);
+            const float tot = subtile_total<T, QP>(d, t, a.V, a.c);
             if (lane == 0) sums[t] = tot;
         }
     }
@@ -375,7 +427,7 @@ __device__ __forceinline__ void draw_run(const FinalArgs &a, int b, int t0, int 
                static_cast<unsigned>(a.NS);
     last = __shfl_sync(0xFFFFFFFFu, last, 0);
     __syncwarp();
-    if (last) finish_sequence<T>(a, b);
+    if (last) finish_sequence<T, QP>(a, b);
 }
 
 }  // namespace

@@ -22,8 +22,8 @@ namespace {
 
 // Persistent grid: warp w sums its even share of the sub-tiles in the
 // flattened (sequence, sub-tile) order, and reports them once per sequence.
-template <typename T>
-__global__ void __launch_bounds__(kThreads, sizeof(T) == 2 ? 3 : 2) final_kernel(const FinalArgs a) {
+template <typename T, bool QP>
+__global__ void __launch_bounds__(kThreads, sizeof(T) == 2 && !QP ? 3 : 2) final_kernel(const FinalArgs a) {
     // Wait until the row kernel has finished and its writes are visible.
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const long long w = static_cast<long long>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
@@ -40,7 +40,7 @@ __global__ void __launch_bounds__(kThreads, sizeof(T) == 2 ? 3 : 2) final_kernel
                                             ? i1 - static_cast<long long>(b) * a.NS
                                             : a.NS);
         i += t1 - t0;
-        draw_run<T>(a, b, t0, t1);
+        draw_run<T, QP>(a, b, t0, t1);
     }
 }
 
@@ -140,12 +140,10 @@ __global__ void intermediates_kernel(const Workspace ws, int B, int k, float *P,
 
 int status() { return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA; }
 
-}  // namespace
-
-int launch_final(const FinalArgs &in, int dtype, cudaStream_t st) {
+template <typename T, bool QP>
+int launch_final_t(const FinalArgs &in, cudaStream_t st) {
     FinalArgs a = in;
-    const int ctas = dtype == SPEC_F32 ? resident_ctas(final_kernel<float>, 4)
-                                       : resident_ctas(final_kernel<uint16_t>, 5);
+    const int ctas = resident_ctas(final_kernel<T, QP>, (sizeof(T) == 2 ? 5 : 4) + (QP ? 2 : 0));
     if (ctas <= 0) return SPEC_ERR_CUDA;
     // a.per carries the grid's warp count W: every resident warp takes an
     // even share (at least one sub-tile each).
@@ -163,9 +161,16 @@ int launch_final(const FinalArgs &in, int dtype, cudaStream_t st) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = dtype == SPEC_F32 ? cudaLaunchKernelEx(&cfg, final_kernel<float>, a)
-                                            : cudaLaunchKernelEx(&cfg, final_kernel<uint16_t>, a);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, final_kernel<T, QP>, a);
     return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+}  // namespace
+
+int launch_final(const FinalArgs &a, int dtype, cudaStream_t st) {
+    if (dtype == SPEC_F32)
+        return a.qprob ? launch_final_t<float, true>(a, st) : launch_final_t<float, false>(a, st);
+    return a.qprob ? launch_final_t<uint16_t, true>(a, st) : launch_final_t<uint16_t, false>(a, st);
 }
 
 int launch_tree(const TreeArgs &a, cudaStream_t st) {

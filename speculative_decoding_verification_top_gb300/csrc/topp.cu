@@ -575,16 +575,21 @@ __global__ void __launch_bounds__(kTpThreads, 3) topp_kernel(const ToppArgs a) {
             const bool ok = na2 <= kAList && nn <= min(kElemCap, kNucCap);
             const int tr = bq * (kk + 1) + rq;
             uint4 *L = a.ws.nuc + static_cast<size_t>(tr) * kNucCap;
-            const T *drow = rq < kk ? static_cast<const T *>(a.rows.draft) +
-                                          (static_cast<size_t>(bq) * kk + rq) * V
-                                    : nullptr;
+            // The draft value at each index: a logit, or (draft given as
+            // probabilities) q itself.
+            const size_t doff = (static_cast<size_t>(bq) * kk + rq) * V;
+            const T *drow = rq < kk && !a.seq.qprob ? static_cast<const T *>(a.rows.draft) + doff
+                                                    : nullptr;
+            const float *dprob = rq < kk && a.seq.qprob
+                                     ? static_cast<const float *>(a.rows.draft) + doff
+                                     : nullptr;
             if (ok) {
                 const int *ix = sh.nidx;
                 for (int i = tid; i < nn; i += kTpThreads) {
                     const int xi = ix[i];
                     int rank = 0;
                     for (int t = 0; t < nn; ++t) rank += ix[t] < xi;
-                    const float lq = drow ? to_f32(drow[xi]) : 0.0f;
+                    const float lq = drow ? to_f32(drow[xi]) : dprob ? dprob[xi] : 0.0f;
                     L[rank] = make_uint4(static_cast<uint32_t>(xi), __float_as_uint(sh.elems[i]),
                                          __float_as_uint(lq), 0u);
                 }

@@ -110,6 +110,34 @@ def gumbel_draw(rng, logits_f32, T, top=None):
     return out.reshape(l.shape[:-1])
 
 
+def draft_prob_rows(rng, target_f32, k, favoured=64, boost=2e5, alpha=0.3):
+    """Draft probability rows [B, k, V] fp32 and tokens drawn from them, for
+    the form of the step that takes the draft as probabilities.
+
+    Input synthesis only: each row is Gamma(alpha) noise, multiplied on the
+    `favoured` largest target logits of the same position by boost / r^1.5
+    (r = 1, 2, ... their rank), so that drafts agree with the target often
+    enough to be accepted; then scaled to sum 1 in fp64 and stored as fp32.
+    Each draft token is drawn from its stored row with numpy's categorical
+    sampler."""
+    t = np.asarray(target_f32)
+    B, _, V = t.shape
+    q = np.empty((B, k, V), np.float32)
+    toks = np.empty((B, k), np.int32)
+    m = min(favoured, V)
+    ramp = boost / np.arange(1, m + 1, dtype=np.float64) ** 1.5
+    for b in range(B):
+        for i in range(k):
+            w = rng.gamma(alpha, 1.0, V)
+            top = np.argpartition(-t[b, i], m - 1)[:m]
+            top = top[np.argsort(-t[b, i][top], kind="stable")]
+            w[top] *= ramp
+            q[b, i] = w / w.sum()
+            row = q[b, i].astype(np.float64)
+            toks[b, i] = rng.choice(V, p=row / row.sum())
+    return q, toks
+
+
 # ---------------------------------------------------------------- workloads
 
 @dataclass
