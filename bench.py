@@ -42,9 +42,15 @@ import workloads  # noqa: E402
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 7900.0
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "stream_kernel_c3.md")
-KERNEL_SOURCES = [os.path.join(ROOT, "speculative_decoding_verification_top_gb300", "csrc", f)
-                  for f in ("common.cuh", "stream.cuh", "rows.cu")]
+_CSRC = os.path.join(ROOT, "speculative_decoding_verification_top_gb300", "csrc")
+# The committed ncu summary of each row-phase kernel, and the sources whose
+# hash it was taken on (its traffic is reported only while they match).
+PROFILES = {
+    "stream_kernel": (os.path.join(ROOT, "profiles", "stream_kernel_c3.md"),
+                      [os.path.join(_CSRC, f) for f in ("common.cuh", "stream.cuh", "rows.cu")]),
+    "topp_kernel": (os.path.join(ROOT, "profiles", "topp_kernel_c4.md"),
+                    [os.path.join(_CSRC, f) for f in ("common.cuh", "topp.cu")]),
+}
 
 
 def parse():
@@ -165,23 +171,26 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def profiled_traffic():
-    """dram bytes per rows_kernel launch from the committed ncu summary, if it
-    was taken on the current kernel source (else None)."""
+def profiled_traffic(kernel, config):
+    """dram bytes per launch of `kernel` from its committed ncu summary, if
+    that was taken on this workload and on the current kernel source (else
+    None)."""
+    summary, sources = PROFILES[kernel]
     try:
-        text = open(PROFILE_SUMMARY).read()
+        text = open(summary).read()
         h = hashlib.sha256()
-        for path in KERNEL_SOURCES:
+        for path in sources:
             h.update(open(path, "rb").read())
         src = h.hexdigest()[:16]
     except OSError:
         return None
     fields = {}
     for line in text.splitlines():
-        if line.startswith("traffic_bytes_per_launch:") or line.startswith("source_sha256_16:"):
+        if line.split(":", 1)[0] in ("traffic_bytes_per_launch", "source_sha256_16", "workload"):
             k, v = line.split(":", 1)
             fields[k.strip()] = v.strip()
-    if fields.get("source_sha256_16") != src or "traffic_bytes_per_launch" not in fields:
+    if (fields.get("source_sha256_16") != src or fields.get("workload") != config
+            or "traffic_bytes_per_launch" not in fields):
         return None
     return float(fields["traffic_bytes_per_launch"])
 
@@ -333,6 +342,40 @@ def timed_acceptance(job, launches=200):
     return out
 
 
+def timed_probs(job, launches=200):
+    """spec_verify_sample_probs on the same target logits with the draft
+    given as fp32 probability rows (seeded synthetic rows, drawn once):
+    device time per call.  Bytes counted: the k+1 target rows of every
+    sequence, plus the fp32 draft row the final draw reads for each
+    sequence that rejected (its residual)."""
+    import torch
+    wl, sv = job.wl, job.sv
+    rng = np.random.default_rng(20240)
+    q, toks = workloads.draft_prob_rows(rng, workloads.as_f32(wl.target), wl.k)
+    qd, xd = to_dev(q, job.dev), to_dev(toks, job.dev)
+
+    def one(i):
+        t, _, _, u = job.sets[i % 2]
+        sv.spec_verify_sample_probs(t.data_ptr(), qd.data_ptr(), xd.data_ptr(), u.data_ptr(),
+                                    wl.B, wl.k, wl.V, wl.T, wl.top_p, job.dtype,
+                                    job.out_t.data_ptr(), job.out_n.data_ptr(),
+                                    job.ws.data_ptr(), job.ws.numel(), job.stream.cuda_stream)
+
+    for i in range(3):
+        one(i)
+    torch.cuda.synchronize()
+    ms = device_launch_ms(one, launches, job.stream)
+    n = job.out_n.cpu().numpy()
+    esz = 2 if wl.dtype == workloads.BF16 else 4
+    nbytes = wl.B * (wl.k + 1) * wl.V * esz + int(((n >= 0) & (n < wl.k)).sum()) * wl.V * 4
+    job.step(0)  # leave the workspace as a logits call left it
+    torch.cuda.synchronize()
+    return {"entry": "spec_verify_sample_probs", "launches": launches,
+            "avg_call_us": round(ms * 1e3, 2), "bytes": nbytes,
+            "achieved_gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
+            "accepted_hist": np.bincount(np.maximum(n, 0), minlength=wl.k + 1).tolist()}
+
+
 def timed_e2e(job, steps):
     """Host buffers -> device -> library call -> results back to the host."""
     import torch
@@ -422,6 +465,7 @@ def run_ours(args):
     total_ms, rows_ms = timed_device(job, args.steps, args.warmup, world)
     clk = clocks.stop()
     accept = timed_acceptance(job) if mode != "tree" else None
+    probs = timed_probs(job) if mode != "tree" else None
     total_ms = max_over_ranks(total_ms, world)
 
     nbytes = wl.logit_bytes(mode)
@@ -433,14 +477,15 @@ def run_ours(args):
     e2e_value = world * nbytes * args.e2e_steps / (e2e_ms * 1e-3) / 1e9
 
     if rows_ms is not None:
-        # The row phase: one stream_kernel launch, or with top-p the
-        # stream_kernel and topp_kernel pair (timed together).
-        topp = wl.top_p < 1.0
+        # The row phase: one stream_kernel launch, or with top-p one
+        # topp_kernel launch.
+        kern = "topp_kernel" if wl.top_p < 1.0 else "stream_kernel"
         achieved = nbytes / (rows_ms * 1e-3) / 1e9
-        roofline = {"bound": "hbm", "kernel": "stream_kernel+topp_kernel" if topp else "stream_kernel",
+        roofline = {"bound": "hbm", "kernel": kern,
                     "achieved": round(achieved, 1),
                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                    "frac": round(achieved / peak, 4), "traffic": None if topp else profiled_traffic(),
+                    "frac": round(achieved / peak, 4),
+                    "traffic": profiled_traffic(kern, args.config),
                     "algorithmic_bytes": nbytes, "avg_launch_us": round(rows_ms * 1e3, 2)}
     else:
         per_launch_ms = ms_step  # the tree call: argmax rows kernel dominates
@@ -474,6 +519,9 @@ def run_ours(args):
         if "achieved_gbs" in accept:
             accept["frac"] = round(accept["achieved_gbs"] / peak, 4)
         out["acceptance"] = accept
+    if probs is not None:
+        probs["frac"] = round(probs["achieved_gbs"] / peak, 4)
+        out["draft_probs"] = probs
     if rank == 0 and world == 1:
         out["cpu_baseline"] = cpu_baseline(wl, mode, args.cpu_seconds)
     if rank == 0:
