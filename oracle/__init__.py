@@ -75,6 +75,8 @@ def _load():
         lib.oracle_verify_sample_probs.restype = I
         lib.oracle_acceptance.argtypes = [P, P, I, I, I, I, D, D, P, P]
         lib.oracle_acceptance.restype = I
+        lib.oracle_tree_mask.argtypes = [P, P, I, I, P, P]
+        lib.oracle_tree_mask.restype = I
         lib.oracle_ancestor_mask.argtypes = [P, I, P]
         lib.oracle_ancestor_mask.restype = I
         lib.oracle_verify_tree.argtypes = [P, I, P, P, I, I, I, I, P, P, P]
@@ -216,6 +218,21 @@ def ancestor_mask(parents):
     mask = np.zeros((N, N), np.uint8)
     st = _load().oracle_ancestor_mask(_ptr(par), N, _ptr(mask))
     return st, mask
+
+
+def tree_mask(parents, pos0=None):
+    """Tree attention mask [B, N, N] (uint8, 1 = may attend: self and
+    ancestors) and positions [B, N] (pos0[b] + depth) for parents [B, N].
+    Returns dict(mask, pos, errors)."""
+    par = np.ascontiguousarray(parents, np.int32)
+    B, N = par.shape
+    p0 = None if pos0 is None else np.ascontiguousarray(pos0, np.int32).reshape(B)
+    mask = np.zeros((B, N, N), np.uint8)
+    pos = np.zeros((B, N), np.int32)
+    err = _load().oracle_tree_mask(_ptr(par), _ptr(p0), B, N, _ptr(mask), _ptr(pos))
+    if err < 0:
+        raise ValueError("oracle_tree_mask rejected its arguments")
+    return dict(mask=mask, pos=pos, errors=err)
 
 
 def verify_tree(target, parents, node_tokens, depth):

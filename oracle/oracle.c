@@ -563,6 +563,52 @@ int oracle_ancestor_mask(const int32_t *parents, int N, uint8_t *mask)
 }
 
 /*
+ * Tree attention inputs for B candidate trees (the step just before the
+ * target pass that verify reads): [LZ] "Tree verification" -- every node
+ * attends to the context and to its own ancestors only, and nodes at the
+ * same depth get the same position index (for RoPE); [LB] "Tree-Based
+ * Verification and Custom Attention Masks": M_ij = 0 where j is an
+ * ancestor of i, -inf elsewhere.
+ *
+ * parents [B, N]  each sequence's tree, as for oracle_verify_tree
+ * pos0    [B]     position index of each tree's root (NULL: all 0)
+ * mask    [B, N, N] (optional): 1 iff j == i or j is an ancestor of i
+ * pos     [B, N]  (optional): pos0[b] + depth(n)
+ * A sequence whose parents are not a rooted tree in topological order gets
+ * an all-zero mask and positions -1.  Returns ORC_BAD_ARGUMENT, or the OR
+ * of (1 << ORC_TREE_SHAPE) if any tree failed.
+ */
+int oracle_tree_mask(const int32_t *parents, const int32_t *pos0, int B, int N,
+                     uint8_t *mask, int32_t *pos)
+{
+    if (!parents || B < 0 || N < 1) return ORC_BAD_ARGUMENT;
+    int32_t *depth = (int32_t *)malloc((size_t)N * sizeof *depth);
+    int errors = 0;
+    for (int b = 0; b < B; ++b) {
+        const int32_t *par = parents + (size_t)b * N;
+        uint8_t *m = mask ? mask + (size_t)b * N * N : NULL;
+        int32_t *pb = pos ? pos + (size_t)b * N : NULL;
+        int status = tree_depths(par, N, depth);
+        if (status != ORC_OK) {
+            errors |= 1 << status;
+            if (m) memset(m, 0, (size_t)N * N);
+            if (pb)
+                for (int n = 0; n < N; ++n) pb[n] = -1;
+            continue;
+        }
+        if (m) {
+            memset(m, 0, (size_t)N * N);
+            for (int i = 0; i < N; ++i)
+                for (int a = i; a >= 0; a = par[a]) m[(size_t)i * N + a] = 1;
+        }
+        if (pb)
+            for (int n = 0; n < N; ++n) pb[n] = (pos0 ? pos0[b] : 0) + depth[n];
+    }
+    free(depth);
+    return errors;
+}
+
+/*
  * Greedy tree verification ([LZ] "Tree verification": keep the longest
  * accepted root-to-leaf path; [LB] "Tree-Based Verification"), reading R6.
  *
