@@ -376,6 +376,37 @@ def timed_probs(job, launches=200):
             "accepted_hist": np.bincount(np.maximum(n, 0), minlength=wl.k + 1).tolist()}
 
 
+def timed_tree_mask(job, launches=200):
+    """spec_verify_tree_mask: the workload's tree for each of its B
+    sequences, and a large case (64 complete 4-ary trees of 1024 nodes,
+    depth 5); mask and positions; device time per call and the bytes
+    written."""
+    import torch
+    wl, sv = job.wl, job.sv
+    out = {}
+    big = np.broadcast_to(((np.arange(1024) - 1) // 4).astype(np.int32), (64, 1024)).copy()
+    big[:, 0] = -1
+    cases = [("workload", np.broadcast_to(wl.parents, (wl.B, wl.N)).copy()), ("B64_N1024", big)]
+    for name, par in cases:
+        B, N = par.shape
+        p = to_dev(par, job.dev)
+        mask = torch.empty((B, N, N), dtype=torch.uint8, device=job.dev)
+        pos = torch.empty((B, N), dtype=torch.int32, device=job.dev)
+
+        def one(i):
+            sv.spec_verify_tree_mask(p.data_ptr(), None, B, N, mask.data_ptr(), None,
+                                     pos.data_ptr(), job.stream.cuda_stream)
+
+        for i in range(3):
+            one(i)
+        torch.cuda.synchronize()
+        ms = device_launch_ms(one, launches, job.stream)
+        nbytes = B * N * N + 4 * B * N + 4 * B * N  # mask + positions written, parents read
+        out[name] = {"B": B, "N": N, "avg_call_us": round(ms * 1e3, 2), "bytes": nbytes,
+                     "achieved_gbs": round(nbytes / (ms * 1e-3) / 1e9, 1)}
+    return out
+
+
 def timed_e2e(job, steps):
     """Host buffers -> device -> library call -> results back to the host."""
     import torch
@@ -466,6 +497,7 @@ def run_ours(args):
     clk = clocks.stop()
     accept = timed_acceptance(job) if mode != "tree" else None
     probs = timed_probs(job) if mode != "tree" else None
+    tmask = timed_tree_mask(job) if mode == "tree" else None
     total_ms = max_over_ranks(total_ms, world)
 
     nbytes = wl.logit_bytes(mode)
@@ -519,6 +551,8 @@ def run_ours(args):
         if "achieved_gbs" in accept:
             accept["frac"] = round(accept["achieved_gbs"] / peak, 4)
         out["acceptance"] = accept
+    if tmask is not None:
+        out["tree_mask"] = tmask
     if probs is not None:
         probs["frac"] = round(probs["achieved_gbs"] / peak, 4)
         out["draft_probs"] = probs

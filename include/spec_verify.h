@@ -238,6 +238,37 @@ int spec_verify_tree(const void *target_logits, const int32_t *parents,
                      spec_stream_t stream);
 
 /*
+ * Tree attention inputs for B candidate trees -- the step just before the
+ * target pass whose logits spec_verify_tree verifies.  [LZ] "Tree
+ * verification": the flattened tree is scored in one target pass where
+ * every node attends to the context and to its own ancestors only, and
+ * nodes at the same depth share one position index (for RoPE); [LB]
+ * "Tree-Based Verification and Custom Attention Masks": M_ij = 0 where
+ * node j is an ancestor of node i, -inf elsewhere.  A node counts as its
+ * own ancestor here (the diagonal is visible), as in [LZ]'s mask.
+ *
+ * Arguments
+ *   parents    [B, N] int32, device: one tree per sequence, flattened as
+ *              for spec_verify_tree (parents[b][0] = -1, 0 <= parents[b][n]
+ *              < n otherwise)
+ *   pos0       [B] int32, device, or NULL (all 0): position index of each
+ *              tree's root (the last committed token)
+ *   1 <= N <= SPEC_MAX_TREE_NODES, B >= 0
+ *   out_mask   [B, N, N] uint8, device, or NULL: 1 where node i (row) may
+ *              attend to node j (column), 0 elsewhere
+ *   out_bias   [B, N, N] fp32, device, or NULL: the same as 0 / -inf
+ *   out_pos    [B, N] int32, device, or NULL: pos0[b] + depth(n)
+ * The context (the tokens before the root) is visible to every node and is
+ * not part of these outputs.  A sequence whose parents are not a rooted
+ * tree in topological order gets an all-zero mask, an all -inf bias and
+ * positions -1 (no error word: this call takes no workspace).
+ * Returns SPEC_OK or a negative status; nothing is enqueued on error.
+ */
+int spec_verify_tree_mask(const int32_t *parents, const int32_t *pos0, int B, int N,
+                          uint8_t *out_mask, float *out_bias, int32_t *out_pos,
+                          spec_stream_t stream);
+
+/*
  * spec_verify_sample for callers that cannot allocate device memory (no
  * counterpart on the pages: it is a deployment variant).  A serving engine
  * that plans all device memory ahead and forbids allocation on its decode

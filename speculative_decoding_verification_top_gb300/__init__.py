@@ -10,7 +10,8 @@ Entry points (same names as the C ABI):
     spec_verify_workspace_size, spec_verify_tree_workspace_size,
     spec_verify_workspace_init, spec_verify_sample, spec_verify_tree,
     spec_verify_last_error, spec_verify_intermediates,
-    spec_verify_acceptance, spec_verify_sample_probs, spec_verify_status_string
+    spec_verify_acceptance, spec_verify_sample_probs, spec_verify_tree_mask,
+    spec_verify_status_string
 plus tensor-level helpers ``verify_sample`` / ``verify_sample_probs`` /
 ``verify_tree`` / ``acceptance`` that take
 torch CUDA tensors, allocate outputs and a zeroed workspace, and raise on a
@@ -28,7 +29,7 @@ LIB_PATH = os.path.join(_PKG, "libspecverify.so")
 CSRC = os.path.join(_PKG, "csrc")
 SOURCES = [os.path.join(CSRC, f)
            for f in ("api.cu", "rows.cu", "topp.cu", "final.cu", "noalloc.cu",
-                     "accept.cu")]
+                     "accept.cu", "treemask.cu")]
 HEADERS = [os.path.join(CSRC, f) for f in ("common.cuh", "stream.cuh", "draw.cuh")]
 INCLUDE = os.path.join(_ROOT, "include")
 HEADER = os.path.join(INCLUDE, "spec_verify.h")
@@ -58,6 +59,7 @@ EXPORTED = (
     "spec_verify_intermediates",
     "spec_verify_acceptance",
     "spec_verify_sample_probs",
+    "spec_verify_tree_mask",
     "spec_verify_status_string",
 )
 
@@ -120,6 +122,7 @@ def lib():
         L.spec_verify_intermediates.argtypes = [P, Z, I, I, I, P, P, P, P, P]
         L.spec_verify_acceptance.argtypes = [P, P, I, I, I, F, F, I, P, P, P, Z, P]
         L.spec_verify_sample_probs.argtypes = [P, P, P, P, I, I, I, F, F, I, P, P, P, Z, P]
+        L.spec_verify_tree_mask.argtypes = [P, P, I, I, P, P, P, P]
         L.spec_verify_status_string.argtypes = [I]
         L.spec_verify_status_string.restype = ctypes.c_char_p
         for name in EXPORTED[:-1]:
@@ -222,6 +225,12 @@ def spec_verify_sample_probs(target_ptr, draft_probs_ptr, tokens_ptr, uniforms_p
         target_ptr, draft_probs_ptr, tokens_ptr, uniforms_ptr, B, k, V, float(temperature),
         float(top_p), dtype, out_tokens_ptr, out_num_ptr, workspace_ptr, workspace_bytes,
         stream))
+
+
+def spec_verify_tree_mask(parents_ptr, pos0_ptr, B, N, out_mask_ptr, out_bias_ptr, out_pos_ptr,
+                          stream=0):
+    return _check(lib().spec_verify_tree_mask(parents_ptr, pos0_ptr, B, N, out_mask_ptr,
+                                              out_bias_ptr, out_pos_ptr, stream))
 
 
 def spec_verify_status_string(status):
@@ -385,3 +394,21 @@ def acceptance(target, draft, workspace, temperature=1.0, top_p=1.0, out_beta=No
                            _ptr(out_beta), _ptr(out_tv), _ptr(workspace), workspace.numel(),
                            _stream(stream))
     return out_beta, out_tv
+
+
+def tree_mask(parents, pos0=None, mask=True, bias=False, pos=True, stream=None):
+    """Tensor-level spec_verify_tree_mask: parents [B, N] int32 (CUDA).
+    Returns (mask [B, N, N] uint8 or None, bias [B, N, N] fp32 or None,
+    pos [B, N] int32 or None)."""
+    torch = _torch()
+    B, N = parents.shape
+    _need(parents, "parents", torch.int32, (B, N))
+    if pos0 is not None:
+        _need(pos0, "pos0", torch.int32, (B,))
+    dev = parents.device
+    m = torch.empty((B, N, N), dtype=torch.uint8, device=dev) if mask else None
+    bs = torch.empty((B, N, N), dtype=torch.float32, device=dev) if bias else None
+    p = torch.empty((B, N), dtype=torch.int32, device=dev) if pos else None
+    spec_verify_tree_mask(_ptr(parents), _ptr(pos0), B, N, _ptr(m), _ptr(bs), _ptr(p),
+                          _stream(stream))
+    return m, bs, p

@@ -306,6 +306,29 @@ SPEC_EXPORT int spec_verify_tree(const void *target_logits, const int32_t *paren
     return launch_tree(ta, st);
 }
 
+SPEC_EXPORT int spec_verify_tree_mask(const int32_t *parents, const int32_t *pos0, int B, int N,
+                                      uint8_t *out_mask, float *out_bias, int32_t *out_pos,
+                                      spec_stream_t stream) {
+    if (B < 0 || N < 1 || N > SPEC_MAX_TREE_NODES ||
+        static_cast<long long>(B) * ((N + 31) / 32) > INT_MAX)
+        return SPEC_ERR_SHAPE;
+    if (B == 0) return SPEC_OK;
+    if (!parents) return SPEC_ERR_NULL;
+    if (!aligned(parents, 4) || (pos0 && !aligned(pos0, 4)) || (out_bias && !aligned(out_bias, 4)) ||
+        (out_pos && !aligned(out_pos, 4)))
+        return SPEC_ERR_ALIGN;
+    if (!out_mask && !out_bias && !out_pos) return SPEC_OK;
+    TreeMaskArgs a;
+    a.parents = parents;
+    a.pos0 = pos0;
+    a.B = B;
+    a.N = N;
+    a.mask = out_mask;
+    a.bias = out_bias;
+    a.pos = out_pos;
+    return launch_tree_mask(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
 SPEC_EXPORT int spec_verify_last_error(void *workspace, size_t workspace_bytes,
                                        spec_stream_t stream) {
     if (!workspace) return SPEC_ERR_NULL;

@@ -635,6 +635,16 @@ struct AcceptArgs {
     float *tv;         // [B, k] or null
 };
 
+struct TreeMaskArgs {
+    const int32_t *parents;  // [B, N]
+    const int32_t *pos0;     // [B] or null (0)
+    int B, N;
+    uint8_t *mask;           // [B, N, N] or null
+    float *bias;             // [B, N, N] or null
+    int32_t *pos;            // [B, N] or null
+    int rows_per_warp;       // 1..32, set by the launcher
+};
+
 struct TreeArgs {
     const int32_t *parents;
     const int32_t *node_tokens;
@@ -677,6 +687,8 @@ int launch_topp_rows(const ToppArgs &a, int rows_total, int dtype, cudaStream_t 
 // The final kernel is launched as a programmatic dependent of the row kernel.
 int launch_final(const FinalArgs &a, int dtype, cudaStream_t st);
 int launch_tree(const TreeArgs &a, cudaStream_t st);
+// Tree attention mask / bias / positions for B trees (treemask.cu).
+int launch_tree_mask(const TreeMaskArgs &a, cudaStream_t st);
 // Acceptance rate per (sequence, position) from a verify call's row records;
 // masked: the rows carry nucleus keys (top-p).
 int launch_accept(const AcceptArgs &a, int dtype, bool masked, cudaStream_t st);

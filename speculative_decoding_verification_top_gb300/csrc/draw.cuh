@@ -118,14 +118,14 @@ template <typename T, bool QP>
 __device__ __forceinline__ void unpack_q(const QRaw<T, QP> &r, float (&f)[Elem<T>::kPerVec]) {
     if (!QP) {
         unpack<T>(r.v[0], f);
-        return;
-    }
+    } else {
 #pragma unroll
-    for (int i = 0; i < QRaw<T, QP>::N; ++i) {
-        f[4 * i] = __uint_as_float(r.v[i].x);
-        f[4 * i + 1] = __uint_as_float(r.v[i].y);
-        f[4 * i + 2] = __uint_as_float(r.v[i].z);
-        f[4 * i + 3] = __uint_as_float(r.v[i].w);
+        for (int i = 0; i < QRaw<T, QP>::N; ++i) {
+            f[4 * i] = __uint_as_float(r.v[i].x);
+            f[4 * i + 1] = __uint_as_float(r.v[i].y);
+            f[4 * i + 2] = __uint_as_float(r.v[i].z);
+            f[4 * i + 3] = __uint_as_float(r.v[i].w);
+        }
     }
 }
 
