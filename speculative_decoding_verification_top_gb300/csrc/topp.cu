@@ -244,11 +244,28 @@ __device__ __forceinline__ void alist_append(ToppShared &sh, uint32_t mask, cons
         }
 }
 
-// alist_append for one batch of kBatch vectors per lane: element u P + e
-// of a lane lies at index x0 + u 32 P + e.
-template <int P>
+// Element e of a raw 16-byte vector as a float (no dynamic register
+// indexing: the word is picked by selects).
+template <typename T>
+__device__ __forceinline__ float elem_of(const uint4 &v, int e) {
+    if (Elem<T>::kPerVec == 4) {
+        const uint32_t w = e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
+        return __uint_as_float(w);
+    }
+    const int wi = e >> 1;
+    const uint32_t w = wi == 0 ? v.x : wi == 1 ? v.y : wi == 2 ? v.z : v.w;
+    return __uint_as_float((e & 1) ? (w & 0xFFFF0000u) : (w << 16));
+}
+
+// alist_append for one batch of kBatch raw vectors per lane: bit u P + e of
+// `mask` is element e of vector u, at index x0 + u 32 P + e.  Each lane
+// walks only its set bits (typically none or one), so the cost follows the
+// candidates, not the batch size.
+template <typename T>
 __device__ __forceinline__ void alist_append_batch(ToppShared &sh, uint32_t mask,
-                                                   const float (&h)[kBatch * P], int x0) {
+                                                   const uint4 (&q)[kBatch], int x0) {
+    static_assert(kBatch == 4, "vector selects below assume four vectors per lane");
+    constexpr int P = Elem<T>::kPerVec;
     const int lane = threadIdx.x & 31;
     if (!__ballot_sync(0xFFFFFFFFu, mask != 0u)) return;
     const int cnt = __popc(mask);
@@ -263,15 +280,17 @@ __device__ __forceinline__ void alist_append_batch(ToppShared &sh, uint32_t mask
     if (lane == 31) base = atomicAdd(&sh.n_alist, tot);
     base = __shfl_sync(0xFFFFFFFFu, base, 31);
     int pos = base + incl - cnt;
-#pragma unroll
-    for (int i = 0; i < kBatch * P; ++i)
-        if (mask & (1u << i)) {
-            if (pos < kAList) {
-                sh.alist[pos] = h[i];
-                sh.aidx[pos] = x0 + (i / P) * 32 * P + (i % P);
-            }
-            ++pos;
+    while (mask) {
+        const int i = __ffs(mask) - 1;
+        mask &= mask - 1u;
+        const int u = i / P, e = i - u * P;
+        const uint4 v = u == 0 ? q[0] : u == 1 ? q[1] : u == 2 ? q[2] : q[3];
+        if (pos < kAList) {
+            sh.alist[pos] = elem_of<T>(v, e);
+            sh.aidx[pos] = x0 + u * 32 * P + e;
         }
+        ++pos;
+    }
 }
 
 // The float whose okey<float> is k.
@@ -351,7 +370,6 @@ __device__ __forceinline__ void stats_capture(ToppShared &sh, const T *rowp, int
         const float negmc = -__fmul_rn(m_run, c);
         float2 acc = make_float2(0.0f, 0.0f);
         float h[kBatch * P];
-        uint32_t mask = 0u;
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
             float f[P];
@@ -363,13 +381,20 @@ __device__ __forceinline__ void stats_capture(ToppShared &sh, const T *rowp, int
                 acc = add2(acc, make_float2(ex2(x.x), ex2(x.y)));
             }
 #pragma unroll
-            for (int e = 0; e < P; ++e) {
-                h[u * P + e] = f[e];
-                if (f[e] >= thr && f[e] > kNegInf) mask |= 1u << (u * P + e);
-            }
+            for (int e = 0; e < P; ++e) h[u * P + e] = f[e];
         }
         if (sum) s_run = __fadd_rn(s_run, __fadd_rn(acc.x, acc.y));
-        alist_append_batch<P>(sh, mask, h, sp.a0 + (v0 + lane) * P);
+        // The capture mask only where this lane's batch reaches the floor:
+        // past the first batches of a peaked row almost none does.  (A
+        // finite floor excludes -inf logits; with no finite max yet the
+        // floor is +inf.)
+        uint32_t mask = 0u;
+        if (bm >= thr) {
+#pragma unroll
+            for (int i = 0; i < kBatch * P; ++i)
+                if (h[i] >= thr) mask |= 1u << i;
+        }
+        alist_append_batch<T>(sh, mask, q, sp.a0 + (v0 + lane) * P);
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) q[u] = nq[u];
     }
