@@ -266,20 +266,10 @@ __device__ __forceinline__ void alist_append_batch(ToppShared &sh, uint32_t mask
                                                    const uint4 (&q)[kBatch], int x0) {
     static_assert(kBatch == 4, "vector selects below assume four vectors per lane");
     constexpr int P = Elem<T>::kPerVec;
-    const int lane = threadIdx.x & 31;
-    if (!__ballot_sync(0xFFFFFFFFu, mask != 0u)) return;
-    const int cnt = __popc(mask);
-    int incl = cnt;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o) incl += y;
-    }
-    const int tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
-    int base = 0;
-    if (lane == 31) base = atomicAdd(&sh.n_alist, tot);
-    base = __shfl_sync(0xFFFFFFFFu, base, 31);
-    int pos = base + incl - cnt;
+    if (!mask) return;
+    // The list's order does not matter (every later use is a set or an
+    // integer sum): each lane reserves its own slots.
+    int pos = atomicAdd(&sh.n_alist, __popc(mask));
     while (mask) {
         const int i = __ffs(mask) - 1;
         mask &= mask - 1u;
@@ -322,15 +312,15 @@ __device__ __forceinline__ void stats_capture(ToppShared &sh, const T *rowp, int
         if (m_run != kNegInf)
             s_run = __fadd_rn(s_run, ex2(__fmaf_rn(l, c, -__fmul_rn(m_run, c))));
     };
-    // Threshold from the warp's and the CTA's running max.
-    auto floor_now = [&]() {
-        float wm = m_run;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xFFFFFFFFu, wm, o));
-        uint32_t ck = wm > kNegInf ? okey<float>(wm) : 0u;
-        if (lane == 0 && ck) ck = max(ck, atomicMax(&sh.cmax, ck));
-        ck = __shfl_sync(0xFFFFFFFFu, ck, 0);
-        return ck ? __fsub_rn(key_float(ck), tryT) : INFINITY;
+    // Threshold from this lane's and the CTA's running max (either is at
+    // most the row's max, so the floor never exceeds m - tryT).  A lane
+    // whose max grew publishes it with a shared atomic (rare once the row's
+    // top logits have been seen).
+    auto floor_now = [&](bool grew) {
+        if (grew && m_run > kNegInf) atomicMax(&sh.cmax, okey<float>(m_run));
+        const uint32_t ck = *reinterpret_cast<volatile uint32_t *>(&sh.cmax);
+        const float ref = ck ? fmaxf(m_run, key_float(ck)) : m_run;
+        return ref > kNegInf ? __fsub_rn(ref, tryT) : INFINITY;
     };
     // The ragged ends (< one vector each): counted, then appended if >= the floor.
     auto edge = [&](int n0, int n1) {
@@ -339,7 +329,7 @@ __device__ __forceinline__ void stats_capture(ToppShared &sh, const T *rowp, int
             h[0] = to_f32(rowp[n0 + lane]);
             scalar(h[0]);
         }
-        const float fl_now = floor_now();
+        const float fl_now = floor_now(true);
         alist_append<1>(sh, (h[0] >= fl_now && h[0] > kNegInf) ? 1u : 0u, h, n0 + lane);
     };
     edge(sp.e0, sp.a0);
@@ -358,14 +348,16 @@ __device__ __forceinline__ void stats_capture(ToppShared &sh, const T *rowp, int
         }
         const float bm = batch_max<T>(q);
         const bool nan = bm != bm;
+        bool grew = false;
         if (nan) fl |= kFlagNonFinite;
         else if (bm > m_run) {
             s_run = __fmul_rn(s_run, ex2(__fmul_rn(__fsub_rn(m_run, bm), c)));
             m_run = bm;
+            grew = true;
         }
         // Floor after this batch's max is counted (so the batch's own top
         // logits are kept); one unpack feeds the sum and the capture mask.
-        const float thr = floor_now();
+        const float thr = floor_now(grew);
         const bool sum = !nan && m_run != kNegInf;
         const float negmc = -__fmul_rn(m_run, c);
         float2 acc = make_float2(0.0f, 0.0f);
