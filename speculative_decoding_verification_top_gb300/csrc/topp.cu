@@ -601,11 +601,60 @@ __global__ void __launch_bounds__(kTpThreads, 3) topp_kernel(const ToppArgs a) {
                                      ? static_cast<const float *>(a.rows.draft) + doff
                                      : nullptr;
             if (ok) {
-                const int *ix = sh.nidx;
-                for (int i = tid; i < nn; i += kTpThreads) {
-                    const int xi = ix[i];
-                    int rank = 0;
-                    for (int t = 0; t < nn; ++t) rank += ix[t] < xi;
+                // Rank by index without comparing every pair: bucket the
+                // entries by their index (kTpThreads buckets over [0, V)),
+                // scan the bucket counts, place each entry in its bucket,
+                // then count the smaller indices inside its bucket alone.
+                // The histogram's memory is free now: counts, bucket
+                // starts, then the entries in bucket order.
+                static_assert(kElemCap % kTpThreads == 0, "entries per thread");
+                constexpr int kPerT = kElemCap / kTpThreads;
+                int *cnt = reinterpret_cast<int *>(sh.sel.hist);
+                int *start = cnt + kTpThreads;
+                int *byb = start + kTpThreads;
+                static_assert(sizeof(sh.sel.hist) >= sizeof(int) * (2 * kTpThreads + kElemCap),
+                              "rank scratch");
+                const int lane = tid & 31, warp = tid >> 5;
+                cnt[tid] = 0;
+                __syncthreads();
+                int bk[kPerT], sl[kPerT];
+#pragma unroll
+                for (int r = 0; r < kPerT; ++r) {
+                    const int i = tid + r * kTpThreads;
+                    bk[r] = 0;
+                    sl[r] = 0;
+                    if (i < nn) {
+                        bk[r] = static_cast<int>((static_cast<long long>(sh.nidx[i]) * kTpThreads) / V);
+                        sl[r] = atomicAdd(&cnt[bk[r]], 1);
+                    }
+                }
+                __syncthreads();
+                const int cb = cnt[tid];
+                int incl = cb;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                    if (lane >= o) incl += y;
+                }
+                if (lane == 31) sh.sel.wsum[warp] = static_cast<unsigned long long>(incl);
+                __syncthreads();
+                int off = 0;
+                for (int w = 0; w < warp; ++w) off += static_cast<int>(sh.sel.wsum[w]);
+                start[tid] = off + incl - cb;
+                __syncthreads();
+#pragma unroll
+                for (int r = 0; r < kPerT; ++r) {
+                    const int i = tid + r * kTpThreads;
+                    if (i < nn) byb[start[bk[r]] + sl[r]] = sh.nidx[i];
+                }
+                __syncthreads();
+#pragma unroll
+                for (int r = 0; r < kPerT; ++r) {
+                    const int i = tid + r * kTpThreads;
+                    if (i >= nn) continue;
+                    const int xi = sh.nidx[i], s0 = start[bk[r]], nb = cnt[bk[r]];
+                    int rank = s0;
+                    for (int t = 0; t < nb; ++t) rank += byb[s0 + t] < xi;
                     const float lq = drow ? to_f32(drow[xi]) : dprob ? dprob[xi] : 0.0f;
                     L[rank] = make_uint4(static_cast<uint32_t>(xi), __float_as_uint(sh.elems[i]),
                                          __float_as_uint(lq), 0u);
