@@ -367,21 +367,41 @@ __device__ __forceinline__ float list_weight(uint4 e, float c, bool use_p, float
     return fmaxf(__fsub_rn(p, q), 0.0f);
 }
 
-// Total weight over a nucleus list: rounds of 32 entries in index order,
-// each round's total as warp_excl_scan defines it, folded in order.
+constexpr int kListRun = 8;  // nucleus-list entries per lane per round (256 per round)
+
+// Weights of one lane's run of kListRun consecutive entries from i0 (zero
+// past n); all loads issued before any arithmetic.
+template <typename T, bool QP>
+__device__ __forceinline__ void list_run(const uint4 *L, int n, int i0, float c, bool use_p,
+                                         float pneg, float pinv, uint32_t plam, float qneg,
+                                         float qinv, uint32_t qlam, float (&w)[kListRun]) {
+    uint4 e[kListRun];
+#pragma unroll
+    for (int t = 0; t < kListRun; ++t)
+        e[t] = i0 + t < n ? __ldcg(L + i0 + t) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int t = 0; t < kListRun; ++t)
+        w[t] = i0 + t < n ? list_weight<T, QP>(e[t], c, use_p, pneg, pinv, plam, qneg, qinv, qlam)
+                          : 0.0f;
+}
+
+// Total weight over a nucleus list: rounds of 32 runs of kListRun entries
+// in index order; a run's weights are added in order, the runs of a round
+// by warp_excl_scan's association, the rounds in order.
 template <typename T, bool QP>
 __device__ float list_total(const uint4 *L, int n, float c, bool use_p, float pneg, float pinv,
                             uint32_t plam, float qneg, float qinv, uint32_t qlam) {
     const int lane = threadIdx.x & 31;
     float S = 0.0f;
-#pragma unroll 4
-    for (int r0 = 0; r0 < n; r0 += 32) {
-        const int i = r0 + lane;
-        const float w = i < n ? list_weight<T, QP>(__ldcg(L + i), c, use_p, pneg, pinv, plam,
-                                                   qneg, qinv, qlam)
-                              : 0.0f;
+    for (int r0 = 0; r0 < n; r0 += 32 * kListRun) {
+        float w[kListRun];
+        list_run<T, QP>(L, n, r0 + lane * kListRun, c, use_p, pneg, pinv, plam, qneg, qinv, qlam,
+                        w);
+        float v = 0.0f;
+#pragma unroll
+        for (int t = 0; t < kListRun; ++t) v = __fadd_rn(v, w[t]);
         float rt;
-        warp_excl_scan(w, rt);
+        warp_excl_scan(v, rt);
         S = __fadd_rn(S, rt);
     }
     return S;
@@ -415,26 +435,37 @@ __device__ bool list_draw(const RowView &v, const SeqArgs &sa, const Workspace &
         S = list_total<T, QP>(L, n, c, use_p, pneg, pinv, plam, qneg, qinv, qlam);
     }
     const float target = __fmul_rn(sa.uniforms[static_cast<size_t>(b) * (k + 1) + k], S);
+    // The same rounds and association as list_total: the first entry with
+    // w > 0 whose cumulative weight exceeds u S, else the last with w > 0.
     float Rsum = 0.0f;
-    int token = -1, lastpos = -1;
-    for (int r0 = 0; r0 < n && token < 0; r0 += 32) {
-        const int i = r0 + lane;
-        uint4 e = make_uint4(0u, 0u, 0u, 0u);
-        float w = 0.0f;
-        if (i < n) {
-            e = __ldcg(L + i);
-            w = list_weight<T, QP>(e, c, use_p, pneg, pinv, plam, qneg, qinv, qlam);
-        }
+    int pos = -1, lastpos = -1;
+    for (int r0 = 0; r0 < n && pos < 0; r0 += 32 * kListRun) {
+        const int i0 = r0 + lane * kListRun;
+        float w[kListRun];
+        list_run<T, QP>(L, n, i0, c, use_p, pneg, pinv, plam, qneg, qinv, qlam, w);
+        float rsum = 0.0f;
+#pragma unroll
+        for (int t = 0; t < kListRun; ++t) rsum = __fadd_rn(rsum, w[t]);
         float rt;
-        const float excl = warp_excl_scan(w, rt);
-        const bool hit = w > 0.0f && __fadd_rn(Rsum, __fadd_rn(excl, w)) > target;
-        const unsigned hm = __ballot_sync(0xFFFFFFFFu, hit);
-        if (hm) token = __shfl_sync(0xFFFFFFFFu, static_cast<int>(e.x), __ffs(hm) - 1);
-        const unsigned nz = __ballot_sync(0xFFFFFFFFu, w > 0.0f);
-        if (nz) lastpos = __shfl_sync(0xFFFFFFFFu, static_cast<int>(e.x), 31 - __clz(nz));
+        const float excl = warp_excl_scan(rsum, rt);
+        float run = 0.0f;
+        int found = -1, lastnz = -1;
+#pragma unroll
+        for (int t = 0; t < kListRun; ++t) {
+            run = __fadd_rn(run, w[t]);
+            if (w[t] > 0.0f) {
+                lastnz = i0 + t;
+                if (found < 0 && __fadd_rn(Rsum, __fadd_rn(excl, run)) > target) found = i0 + t;
+            }
+        }
+        const unsigned hm = __ballot_sync(0xFFFFFFFFu, found >= 0);
+        if (hm) pos = __shfl_sync(0xFFFFFFFFu, found, __ffs(hm) - 1);
+        const unsigned nz = __ballot_sync(0xFFFFFFFFu, lastnz >= 0);
+        if (nz) lastpos = __shfl_sync(0xFFFFFFFFu, lastnz, 31 - __clz(nz));
         Rsum = __fadd_rn(Rsum, rt);
     }
-    if (token < 0) token = lastpos;
+    if (pos < 0) pos = lastpos;
+    const int token = pos >= 0 ? static_cast<int>(__ldcg(&L[pos].x)) : -1;
     int32_t *ot = sa.out_tokens + static_cast<size_t>(b) * (k + 1);
     if (lane <= k) {
         int32_t val = -1;
