@@ -65,6 +65,14 @@ def _load():
         I, D = ctypes.c_int, ctypes.c_double
         lib.oracle_process_row.argtypes = [P, I, I, D, D, P, P]
         lib.oracle_process_row.restype = I
+        lib.oracle_process_row_k.argtypes = [P, I, I, D, D, I, P, P]
+        lib.oracle_process_row_k.restype = I
+        lib.oracle_verify_sample_k.argtypes = [P, P, I, P, P, I, I, I, D, D, I, I, P, P, P, P]
+        lib.oracle_verify_sample_k.restype = I
+        lib.oracle_verify_sample_probs_k.argtypes = [P, P, I, P, P, I, I, I, D, D, I, P, P, P, P]
+        lib.oracle_verify_sample_probs_k.restype = I
+        lib.oracle_acceptance_k.argtypes = [P, P, I, I, I, I, D, D, I, P, P]
+        lib.oracle_acceptance_k.restype = I
         lib.oracle_argmax_row.argtypes = [P, I, I, P]
         lib.oracle_argmax_row.restype = I
         lib.oracle_inverse_cdf.argtypes = [P, I, D, P]
@@ -98,8 +106,8 @@ def _logits(a):
     raise TypeError("logits must be float32 or uint16 (bf16 bit patterns), got %s" % a.dtype)
 
 
-def process_row(logits, T: float = 1.0, top_p: float = 1.0):
-    """Processed distribution of one row (temperature, then top-p).
+def process_row(logits, T: float = 1.0, top_p: float = 1.0, top_k: int = 0):
+    """Processed distribution of one row (temperature, top-k, then top-p).
 
     Returns (status, prob[V] float64, info[4]) with info = (Z, tau,
     mass above tau, mass at and above tau).
@@ -108,7 +116,8 @@ def process_row(logits, T: float = 1.0, top_p: float = 1.0):
     V = row.shape[-1]
     prob = np.zeros(V, np.float64)
     info = np.zeros(4, np.float64)
-    st = _load().oracle_process_row(_ptr(row), dt, V, float(T), float(top_p), _ptr(prob), _ptr(info))
+    st = _load().oracle_process_row_k(_ptr(row), dt, V, float(T), float(top_p), int(top_k),
+                                      _ptr(prob), _ptr(info))
     return st, prob, info
 
 
@@ -128,7 +137,7 @@ def inverse_cdf(w, u: float):
 
 
 def verify_sample(target, draft, draft_tokens, uniforms, T=1.0, top_p=1.0, mode=STOCHASTIC,
-                  debug=False):
+                  debug=False, top_k=0):
     """One verification step for B sequences.
 
     target [B, k+1, V], draft [B, k, V] (None in GREEDY), draft_tokens [B, k]
@@ -152,9 +161,9 @@ def verify_sample(target, draft, draft_tokens, uniforms, T=1.0, top_p=1.0, mode=
     dbg = np.zeros((B, 2 * k + 3), np.float64) if debug else None
     R = 2 * k + 1 if mode == STOCHASTIC else k + 1
     info = np.zeros((B, R, 4), np.float64) if debug else None
-    err = _load().oracle_verify_sample(
-        _ptr(tgt), _ptr(drf), dt, _ptr(toks), _ptr(uni), B, k, V, float(T), float(top_p), int(mode),
-        _ptr(out_t), _ptr(out_n), _ptr(dbg), _ptr(info))
+    err = _load().oracle_verify_sample_k(
+        _ptr(tgt), _ptr(drf), dt, _ptr(toks), _ptr(uni), B, k, V, float(T), float(top_p),
+        int(top_k), int(mode), _ptr(out_t), _ptr(out_n), _ptr(dbg), _ptr(info))
     if err < 0:
         raise ValueError("oracle_verify_sample rejected its arguments")
     res = dict(tokens=out_t, num_accepted=out_n, errors=err)
@@ -164,7 +173,7 @@ def verify_sample(target, draft, draft_tokens, uniforms, T=1.0, top_p=1.0, mode=
 
 
 def verify_sample_probs(target, draft_probs, draft_tokens, uniforms, T=1.0, top_p=1.0,
-                        debug=False):
+                        debug=False, top_k=0):
     """verify_sample with the draft given as probabilities: draft_probs
     [B, k, V] float32 is q itself (used as given; temperature and top-p
     process the target rows only).  Same results; with debug=True row_info
@@ -181,9 +190,9 @@ def verify_sample_probs(target, draft_probs, draft_tokens, uniforms, T=1.0, top_
     out_n = np.zeros(B, np.int32)
     dbg = np.zeros((B, 2 * k + 3), np.float64) if debug else None
     info = np.zeros((B, k + 1, 4), np.float64) if debug else None
-    err = _load().oracle_verify_sample_probs(
+    err = _load().oracle_verify_sample_probs_k(
         _ptr(tgt), _ptr(q), dt, _ptr(toks), _ptr(uni), B, k, V, float(T), float(top_p),
-        _ptr(out_t), _ptr(out_n), _ptr(dbg), _ptr(info))
+        int(top_k), _ptr(out_t), _ptr(out_n), _ptr(dbg), _ptr(info))
     if err < 0:
         raise ValueError("oracle_verify_sample_probs rejected its arguments")
     res = dict(tokens=out_t, num_accepted=out_n, errors=err)
@@ -192,7 +201,7 @@ def verify_sample_probs(target, draft_probs, draft_tokens, uniforms, T=1.0, top_
     return res
 
 
-def acceptance(target, draft, T=1.0, top_p=1.0):
+def acceptance(target, draft, T=1.0, top_p=1.0, top_k=0):
     """Per-position acceptance rate beta [B, k] = sum_x min(p_i, q_i) and
     total-variation distance tv [B, k] = (1/2) sum_x |p_i - q_i|, each from
     its own definition.  target [B, k+1, V], draft [B, k, V].
@@ -205,8 +214,8 @@ def acceptance(target, draft, T=1.0, top_p=1.0):
         raise ValueError("draft logits must match target dtype and be [B, k, V]")
     beta = np.zeros((B, k), np.float64)
     tv = np.zeros((B, k), np.float64)
-    err = _load().oracle_acceptance(_ptr(tgt), _ptr(drf), dt, B, k, V, float(T), float(top_p),
-                                    _ptr(beta), _ptr(tv))
+    err = _load().oracle_acceptance_k(_ptr(tgt), _ptr(drf), dt, B, k, V, float(T), float(top_p),
+                                      int(top_k), _ptr(beta), _ptr(tv))
     if err < 0:
         raise ValueError("oracle_acceptance rejected its arguments")
     return dict(beta=beta, tv=tv, errors=err)

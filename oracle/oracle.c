@@ -46,6 +46,12 @@
  *   R7 data errors: a row holding NaN or +inf, a row that is entirely -inf,
  *      a token outside [0, V) or a uniform outside [0, 1) marks the whole
  *      sequence as failed: its tokens and its accepted count are -1.
+ *   R10 top-k ([MN] 6 "Pitfalls" names top-k among the processors the
+ *      target and draft must share; never defined): keep the tokens whose
+ *      logit is at least the K-th largest logit of the row (all ties of the
+ *      K-th kept, as in R1), renormalise; applied after temperature (which
+ *      does not change the order) and before top-p, which then runs on the
+ *      renormalised top-k distribution.  K <= 0 or K >= V: no top-k.
  *   R8 draft given as probabilities: the step takes the draft "logits (or
  *      probabilities)".  Reading: a probability row is q itself, the
  *      distribution the drafter sampled from -- used as given (no
@@ -165,8 +171,31 @@ static void nucleus(double *prob, int V, double top_p, double *info)
  * [3] mass at and above tau (top-p only; tau = 0 and both masses = 1
  * without top-p).
  */
-int oracle_process_row(const void *logits, int dtype, int V, double T,
-                       double top_p, double *prob, double *info)
+/*
+ * Top-k filter of a normalised row, reading R10: the K-th largest value
+ * (counting equal values one by one), every token at or above it kept,
+ * the kept mass renormalised.  Probability is increasing in the logit
+ * (T > 0), so this keeps the K largest logits and their ties.
+ */
+static void top_k_filter(double *prob, int V, int top_k)
+{
+    int32_t *order = (int32_t *)malloc((size_t)V * sizeof *order);
+    for (int v = 0; v < V; ++v) order[v] = v;
+    g_sort_prob = prob;
+    qsort(order, (size_t)V, sizeof *order, by_prob_desc);
+    const double kth = prob[order[top_k - 1]];
+    free(order);
+    double kept = 0.0;
+    for (int v = 0; v < V; ++v) {
+        if (prob[v] < kth) prob[v] = 0.0;
+        kept += prob[v];
+    }
+    for (int v = 0; v < V; ++v) prob[v] /= kept;
+}
+
+/* oracle_process_row with top-k (R10) between temperature and top-p. */
+int oracle_process_row_k(const void *logits, int dtype, int V, double T,
+                         double top_p, int top_k, double *prob, double *info)
 {
     if (!logits || !prob || V < 1 || !(T > 0.0) || !(top_p > 0.0))
         return ORC_BAD_ARGUMENT;
@@ -186,6 +215,7 @@ int oracle_process_row(const void *logits, int dtype, int V, double T,
         Z += e;
     }
     for (int v = 0; v < V; ++v) prob[v] /= Z;
+    if (top_k > 0 && top_k < V) top_k_filter(prob, V, top_k);
 
     double tinfo[3] = {0.0, 1.0, 1.0};
     if (top_p < 1.0) nucleus(prob, V, top_p, tinfo);
@@ -196,6 +226,12 @@ int oracle_process_row(const void *logits, int dtype, int V, double T,
         info[3] = tinfo[2];
     }
     return ORC_OK;
+}
+
+int oracle_process_row(const void *logits, int dtype, int V, double T,
+                       double top_p, double *prob, double *info)
+{
+    return oracle_process_row_k(logits, dtype, V, T, top_p, 0, prob, info);
 }
 
 /* First (lowest-index) maximum of the raw logits, reading R5.  Returns a
@@ -326,11 +362,11 @@ static void step_sequence(const double *p, const double *q, const int32_t *xt,
  * Returns ORC_BAD_ARGUMENT, or the OR of (1 << status) over every check
  * that failed in any sequence (a failed sequence is checked completely).
  */
-int oracle_verify_sample(const void *target, const void *draft, int dtype,
-                         const int32_t *tokens, const float *uniforms,
-                         int B, int k, int V, double T, double top_p,
-                         int mode, int32_t *out_tokens, int32_t *out_num,
-                         double *dbg, double *row_info)
+int oracle_verify_sample_k(const void *target, const void *draft, int dtype,
+                           const int32_t *tokens, const float *uniforms,
+                           int B, int k, int V, double T, double top_p, int top_k,
+                           int mode, int32_t *out_tokens, int32_t *out_num,
+                           double *dbg, double *row_info)
 {
     if (!target || !tokens || !out_tokens || !out_num || B < 0 || k < 1 ||
         V < 1 || (dtype != ORC_F32 && dtype != ORC_BF16) ||
@@ -391,8 +427,8 @@ int oracle_verify_sample(const void *target, const void *draft, int dtype,
                        : (const char *)draft +
                              ((size_t)b * k + (r - k - 1)) * V * esz;
             double *info = row_info ? row_info + ((size_t)b * R + r) * 4 : NULL;
-            int status = oracle_process_row(row, dtype, V, T, top_p,
-                                            prob + (size_t)r * V, info);
+            int status = oracle_process_row_k(row, dtype, V, T, top_p, top_k,
+                                              prob + (size_t)r * V, info);
             if (status != ORC_OK) bad |= 1 << status;
         }
         if (bad) {
@@ -416,11 +452,11 @@ int oracle_verify_sample(const void *target, const void *draft, int dtype,
  * are processed as usual.  Same outputs; row_info [B, k+1, 4] (optional)
  * covers the target rows only.
  */
-int oracle_verify_sample_probs(const void *target, const float *draft_probs,
-                               int dtype, const int32_t *tokens,
-                               const float *uniforms, int B, int k, int V,
-                               double T, double top_p, int32_t *out_tokens,
-                               int32_t *out_num, double *dbg, double *row_info)
+int oracle_verify_sample_probs_k(const void *target, const float *draft_probs,
+                                 int dtype, const int32_t *tokens,
+                                 const float *uniforms, int B, int k, int V,
+                                 double T, double top_p, int top_k, int32_t *out_tokens,
+                                 int32_t *out_num, double *dbg, double *row_info)
 {
     if (!target || !draft_probs || !tokens || !uniforms || !out_tokens ||
         !out_num || B < 0 || k < 1 || V < 1 ||
@@ -451,7 +487,8 @@ int oracle_verify_sample_probs(const void *target, const float *draft_probs,
         for (int r = 0; r <= k; ++r) {
             const char *row = (const char *)target + ((size_t)b * (k + 1) + r) * V * esz;
             double *info = row_info ? row_info + ((size_t)b * (k + 1) + r) * 4 : NULL;
-            int status = oracle_process_row(row, dtype, V, T, top_p, p + (size_t)r * V, info);
+            int status = oracle_process_row_k(row, dtype, V, T, top_p, top_k,
+                                              p + (size_t)r * V, info);
             if (status != ORC_OK) bad |= 1 << status;
         }
         if (bad) {
@@ -487,9 +524,9 @@ int oracle_verify_sample_probs(const void *target, const float *draft_probs,
  *      has a data error (R7)
  * Returns ORC_BAD_ARGUMENT, or the OR of (1 << status) over failed rows.
  */
-int oracle_acceptance(const void *target, const void *draft, int dtype,
-                      int B, int k, int V, double T, double top_p,
-                      double *beta, double *tv)
+int oracle_acceptance_k(const void *target, const void *draft, int dtype,
+                        int B, int k, int V, double T, double top_p, int top_k,
+                        double *beta, double *tv)
 {
     if (!target || !draft || !beta || B < 0 || k < 1 || V < 1 ||
         (dtype != ORC_F32 && dtype != ORC_BF16) || !(T > 0.0) ||
@@ -503,8 +540,8 @@ int oracle_acceptance(const void *target, const void *draft, int dtype,
         for (int i = 0; i < k; ++i) {
             const char *prow = (const char *)target + ((size_t)b * (k + 1) + i) * V * esz;
             const char *qrow = (const char *)draft + ((size_t)b * k + i) * V * esz;
-            int sp = oracle_process_row(prow, dtype, V, T, top_p, p, NULL);
-            int sq = oracle_process_row(qrow, dtype, V, T, top_p, q, NULL);
+            int sp = oracle_process_row_k(prow, dtype, V, T, top_p, top_k, p, NULL);
+            int sq = oracle_process_row_k(qrow, dtype, V, T, top_p, top_k, q, NULL);
             double overlap = NAN, dist = NAN;
             if (sp != ORC_OK) errors |= 1 << sp;
             if (sq != ORC_OK) errors |= 1 << sq;
@@ -524,6 +561,34 @@ int oracle_acceptance(const void *target, const void *draft, int dtype,
     free(p);
     free(q);
     return errors;
+}
+
+/* The same three entry points without top-k. */
+int oracle_verify_sample(const void *target, const void *draft, int dtype,
+                         const int32_t *tokens, const float *uniforms,
+                         int B, int k, int V, double T, double top_p,
+                         int mode, int32_t *out_tokens, int32_t *out_num,
+                         double *dbg, double *row_info)
+{
+    return oracle_verify_sample_k(target, draft, dtype, tokens, uniforms, B, k, V, T, top_p,
+                                  0, mode, out_tokens, out_num, dbg, row_info);
+}
+
+int oracle_verify_sample_probs(const void *target, const float *draft_probs,
+                               int dtype, const int32_t *tokens,
+                               const float *uniforms, int B, int k, int V,
+                               double T, double top_p, int32_t *out_tokens,
+                               int32_t *out_num, double *dbg, double *row_info)
+{
+    return oracle_verify_sample_probs_k(target, draft_probs, dtype, tokens, uniforms, B, k, V,
+                                        T, top_p, 0, out_tokens, out_num, dbg, row_info);
+}
+
+int oracle_acceptance(const void *target, const void *draft, int dtype,
+                      int B, int k, int V, double T, double top_p,
+                      double *beta, double *tv)
+{
+    return oracle_acceptance_k(target, draft, dtype, B, k, V, T, top_p, 0, beta, tv);
 }
 
 /* -------------------------------------------------------- tree verify */
