@@ -320,7 +320,7 @@ def timed_acceptance(job, launches=200):
     def one(i):
         t, d = job.sets[i % 2][:2]
         sv.spec_verify_acceptance(t.data_ptr(), d.data_ptr(), wl.B, wl.k, wl.V, wl.T, wl.top_p,
-                                  job.dtype, beta.data_ptr(), tv.data_ptr(), job.ws.data_ptr(),
+                                  0, job.dtype, beta.data_ptr(), tv.data_ptr(), job.ws.data_ptr(),
                                   job.ws.numel(), job.stream.cuda_stream)
 
     for i in range(3):
@@ -357,7 +357,7 @@ def timed_probs(job, launches=200):
     def one(i):
         t, _, _, u = job.sets[i % 2]
         sv.spec_verify_sample_probs(t.data_ptr(), qd.data_ptr(), xd.data_ptr(), u.data_ptr(),
-                                    wl.B, wl.k, wl.V, wl.T, wl.top_p, job.dtype,
+                                    wl.B, wl.k, wl.V, wl.T, wl.top_p, 0, job.dtype,
                                     job.out_t.data_ptr(), job.out_n.data_ptr(),
                                     job.ws.data_ptr(), job.ws.numel(), job.stream.cuda_stream)
 

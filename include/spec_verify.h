@@ -153,6 +153,24 @@ int spec_verify_sample(const void *target_logits, const void *draft_logits,
                        size_t workspace_bytes, spec_stream_t stream);
 
 /*
+ * spec_verify_sample with top-k as well ([MN] 6 "Pitfalls": target and
+ * draft must share temperature, top-p, top-k and every other logit
+ * processor; the pages never define top-k).  Reading: after temperature,
+ * keep the tokens whose logit is at least the top_k-th largest of the row
+ * (every tie of it kept) and renormalise; top-p then applies to that
+ * renormalised distribution.  top_k <= 0 or top_k >= V: no top-k (the call
+ * is then spec_verify_sample).  Same processing on target and draft rows;
+ * ignored in SPEC_GREEDY mode.  Other arguments and results as for
+ * spec_verify_sample.
+ */
+int spec_verify_sample_topk(const void *target_logits, const void *draft_logits,
+                            const int32_t *draft_tokens, const float *uniforms,
+                            int B, int k, int V, float temperature, float top_p, int top_k,
+                            int mode, int dtype, int32_t *out_tokens,
+                            int32_t *out_num_accepted, void *workspace,
+                            size_t workspace_bytes, spec_stream_t stream);
+
+/*
  * The two phases of spec_verify_sample, with the same arguments.
  * spec_verify_sample == spec_verify_sample_rows followed, on the same
  * stream and workspace, by spec_verify_sample_finish.
@@ -183,8 +201,9 @@ int spec_verify_sample_finish(const void *target_logits, const void *draft_logit
  * probabilities instead of logits: the step takes "draft logits (or
  * probabilities)".  draft_probs [B, k, V] fp32 is q_1..q_k itself -- the
  * distributions the drafter sampled x~_i from -- and is used as given: no
- * temperature, no top-p, no renormalisation.  temperature and top_p
- * process the target rows only (p_i as in spec_verify_sample).  Draft rows
+ * temperature, no top-p, no top-k, no renormalisation.  temperature, top_k
+ * and top_p process the target rows only (p_i as in
+ * spec_verify_sample_topk).  Draft rows
  * are read only where the step needs them: q_i(x~_i) at each draft token,
  * and the rejecting position's row for the residual max(0, p - q).
  *
@@ -203,7 +222,7 @@ int spec_verify_sample_finish(const void *target_logits, const void *draft_logit
 int spec_verify_sample_probs(const void *target_logits, const float *draft_probs,
                              const int32_t *draft_tokens, const float *uniforms,
                              int B, int k, int V, float temperature, float top_p,
-                             int dtype, int32_t *out_tokens, int32_t *out_num_accepted,
+                             int top_k, int dtype, int32_t *out_tokens, int32_t *out_num_accepted,
                              void *workspace, size_t workspace_bytes,
                              spec_stream_t stream);
 
@@ -322,17 +341,19 @@ int spec_verify_intermediates(const void *workspace, size_t workspace_bytes,
  * (1/2) sum_x |p(x) - q(x)|.  Engines log beta to track how well the draft
  * matches the target.
  *
- * Reads the per-row statistics that the last spec_verify_sample (or
- * spec_verify_sample_rows) call left in `workspace`; that call must have
- * been SPEC_STOCHASTIC, with the same target_logits, draft_logits, B, k,
- * V, temperature, top_p and dtype, on this stream (or ordered before it).
+ * Reads the per-row statistics that the last spec_verify_sample,
+ * spec_verify_sample_topk (or spec_verify_sample_rows) call left in
+ * `workspace`; that call must have been SPEC_STOCHASTIC, with the same
+ * target_logits, draft_logits, B, k, V, temperature, top_p, top_k (0 for
+ * spec_verify_sample) and dtype, on this stream (or ordered before it).
  * Otherwise the results are meaningless (never out of bounds).  It changes
  * nothing that spec_verify_sample_finish reads, so it may run between
  * _rows and _finish.
  *
  * Arguments
- *   target_logits, draft_logits, B, k, V, temperature, top_p, dtype: as for
- *                    spec_verify_sample (target rows k+1 are not read)
+ *   target_logits, draft_logits, B, k, V, temperature, top_p, top_k, dtype:
+ *                    as for spec_verify_sample_topk (target rows k+1 are
+ *                    not read)
  *   out_beta         [B, k] fp32, device: beta_i for i = 1..k; NaN where
  *                    row i of the target or draft has a data error
  *   out_tv           [B, k] fp32, device, or NULL: 1 - beta_i
@@ -340,7 +361,7 @@ int spec_verify_intermediates(const void *workspace, size_t workspace_bytes,
  * Returns SPEC_OK or a negative status; nothing is enqueued on error.
  */
 int spec_verify_acceptance(const void *target_logits, const void *draft_logits, int B,
-                           int k, int V, float temperature, float top_p, int dtype,
+                           int k, int V, float temperature, float top_p, int top_k, int dtype,
                            float *out_beta, float *out_tv, void *workspace,
                            size_t workspace_bytes, spec_stream_t stream);
 

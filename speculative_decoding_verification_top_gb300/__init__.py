@@ -51,6 +51,7 @@ EXPORTED = (
     "spec_verify_tree_workspace_size",
     "spec_verify_workspace_init",
     "spec_verify_sample",
+    "spec_verify_sample_topk",
     "spec_verify_sample_rows",
     "spec_verify_sample_finish",
     "spec_verify_sample_noalloc",
@@ -116,12 +117,13 @@ def lib():
         L.spec_verify_workspace_init.argtypes = [P, Z, P]
         for name in ("spec_verify_sample", "spec_verify_sample_rows", "spec_verify_sample_finish"):
             getattr(L, name).argtypes = [P, P, P, P, I, I, I, F, F, I, I, P, P, P, Z, P]
+        L.spec_verify_sample_topk.argtypes = [P, P, P, P, I, I, I, F, F, I, I, I, P, P, P, Z, P]
         L.spec_verify_sample_noalloc.argtypes = [P, P, P, P, I, I, I, F, F, I, I, P, P, P]
         L.spec_verify_tree.argtypes = [P, P, P, I, I, I, I, I, P, P, P, P, Z, P]
         L.spec_verify_last_error.argtypes = [P, Z, P]
         L.spec_verify_intermediates.argtypes = [P, Z, I, I, I, P, P, P, P, P]
-        L.spec_verify_acceptance.argtypes = [P, P, I, I, I, F, F, I, P, P, P, Z, P]
-        L.spec_verify_sample_probs.argtypes = [P, P, P, P, I, I, I, F, F, I, P, P, P, Z, P]
+        L.spec_verify_acceptance.argtypes = [P, P, I, I, I, F, F, I, I, P, P, P, Z, P]
+        L.spec_verify_sample_probs.argtypes = [P, P, P, P, I, I, I, F, F, I, I, P, P, P, Z, P]
         L.spec_verify_tree_mask.argtypes = [P, P, I, I, P, P, P, P]
         L.spec_verify_status_string.argtypes = [I]
         L.spec_verify_status_string.restype = ctypes.c_char_p
@@ -161,6 +163,15 @@ def spec_verify_sample(target_ptr, draft_ptr, tokens_ptr, uniforms_ptr, B, k, V,
     return _check(lib().spec_verify_sample(
         target_ptr, draft_ptr, tokens_ptr, uniforms_ptr, B, k, V, float(temperature),
         float(top_p), mode, dtype, out_tokens_ptr, out_num_ptr, workspace_ptr,
+        workspace_bytes, stream))
+
+
+def spec_verify_sample_topk(target_ptr, draft_ptr, tokens_ptr, uniforms_ptr, B, k, V,
+                            temperature, top_p, top_k, mode, dtype, out_tokens_ptr, out_num_ptr,
+                            workspace_ptr, workspace_bytes, stream=0):
+    return _check(lib().spec_verify_sample_topk(
+        target_ptr, draft_ptr, tokens_ptr, uniforms_ptr, B, k, V, float(temperature),
+        float(top_p), int(top_k), mode, dtype, out_tokens_ptr, out_num_ptr, workspace_ptr,
         workspace_bytes, stream))
 
 
@@ -211,20 +222,20 @@ def spec_verify_intermediates(workspace_ptr, workspace_bytes, B, k, V, P_ptr, Q_
                                                   P_ptr, Q_ptr, Z_ptr, S_ptr, stream))
 
 
-def spec_verify_acceptance(target_ptr, draft_ptr, B, k, V, temperature, top_p, dtype,
+def spec_verify_acceptance(target_ptr, draft_ptr, B, k, V, temperature, top_p, top_k, dtype,
                            out_beta_ptr, out_tv_ptr, workspace_ptr, workspace_bytes, stream=0):
     return _check(lib().spec_verify_acceptance(
-        target_ptr, draft_ptr, B, k, V, float(temperature), float(top_p), dtype, out_beta_ptr,
-        out_tv_ptr, workspace_ptr, workspace_bytes, stream))
+        target_ptr, draft_ptr, B, k, V, float(temperature), float(top_p), int(top_k), dtype,
+        out_beta_ptr, out_tv_ptr, workspace_ptr, workspace_bytes, stream))
 
 
 def spec_verify_sample_probs(target_ptr, draft_probs_ptr, tokens_ptr, uniforms_ptr, B, k, V,
-                             temperature, top_p, dtype, out_tokens_ptr, out_num_ptr,
+                             temperature, top_p, top_k, dtype, out_tokens_ptr, out_num_ptr,
                              workspace_ptr, workspace_bytes, stream=0):
     return _check(lib().spec_verify_sample_probs(
         target_ptr, draft_probs_ptr, tokens_ptr, uniforms_ptr, B, k, V, float(temperature),
-        float(top_p), dtype, out_tokens_ptr, out_num_ptr, workspace_ptr, workspace_bytes,
-        stream))
+        float(top_p), int(top_k), dtype, out_tokens_ptr, out_num_ptr, workspace_ptr,
+        workspace_bytes, stream))
 
 
 def spec_verify_tree_mask(parents_ptr, pos0_ptr, B, N, out_mask_ptr, out_bias_ptr, out_pos_ptr,
@@ -278,7 +289,7 @@ def new_workspace(nbytes, device):
 
 def verify_sample(target, draft, draft_tokens, uniforms, temperature=1.0, top_p=1.0,
                   mode=SPEC_STOCHASTIC, out_tokens=None, out_num=None, workspace=None,
-                  stream=None):
+                  stream=None, top_k=0):
     """Tensor-level spec_verify_sample.  Returns (out_tokens [B, k+1],
     out_num_accepted [B], workspace)."""
     torch = _torch()
@@ -298,15 +309,20 @@ def verify_sample(target, draft, draft_tokens, uniforms, temperature=1.0, top_p=
     nbytes = spec_verify_workspace_size(B, k, V)
     if workspace is None:
         workspace = new_workspace(nbytes, dev)
-    spec_verify_sample(_ptr(target), _ptr(draft) if mode == SPEC_STOCHASTIC else None,
-                       _ptr(draft_tokens), _ptr(uniforms) if mode == SPEC_STOCHASTIC else None,
-                       B, k, V, temperature, top_p, mode, dt, _ptr(out_tokens), _ptr(out_num),
-                       _ptr(workspace), workspace.numel(), _stream(stream))
+    stoch = mode == SPEC_STOCHASTIC
+    args = (_ptr(target), _ptr(draft) if stoch else None, _ptr(draft_tokens),
+            _ptr(uniforms) if stoch else None, B, k, V, temperature, top_p)
+    tail = (mode, dt, _ptr(out_tokens), _ptr(out_num), _ptr(workspace), workspace.numel(),
+            _stream(stream))
+    if top_k:
+        spec_verify_sample_topk(*args, top_k, *tail)
+    else:
+        spec_verify_sample(*args, *tail)
     return out_tokens, out_num, workspace
 
 
 def verify_sample_probs(target, draft_probs, draft_tokens, uniforms, temperature=1.0, top_p=1.0,
-                        out_tokens=None, out_num=None, workspace=None, stream=None):
+                        out_tokens=None, out_num=None, workspace=None, stream=None, top_k=0):
     """Tensor-level spec_verify_sample_probs (draft given as fp32
     probabilities [B, k, V]).  Returns (out_tokens, out_num_accepted,
     workspace)."""
@@ -326,7 +342,8 @@ def verify_sample_probs(target, draft_probs, draft_tokens, uniforms, temperature
     if workspace is None:
         workspace = new_workspace(spec_verify_workspace_size(B, k, V), dev)
     spec_verify_sample_probs(_ptr(target), _ptr(draft_probs), _ptr(draft_tokens), _ptr(uniforms),
-                             B, k, V, temperature, top_p, dt, _ptr(out_tokens), _ptr(out_num),
+                             B, k, V, temperature, top_p, top_k, dt, _ptr(out_tokens),
+                             _ptr(out_num),
                              _ptr(workspace), workspace.numel(), _stream(stream))
     return out_tokens, out_num, workspace
 
@@ -376,7 +393,7 @@ def intermediates(workspace, B, k, V, stream=None):
 
 
 def acceptance(target, draft, workspace, temperature=1.0, top_p=1.0, out_beta=None, out_tv=None,
-               stream=None):
+               stream=None, top_k=0):
     """Tensor-level spec_verify_acceptance: (beta [B, k], tv [B, k]) of the
     last stochastic verify call made on `workspace` with these arguments."""
     torch = _torch()
@@ -390,7 +407,7 @@ def acceptance(target, draft, workspace, temperature=1.0, top_p=1.0, out_beta=No
         out_beta = torch.empty((B, k), dtype=torch.float32, device=dev)
     if out_tv is None:
         out_tv = torch.empty((B, k), dtype=torch.float32, device=dev)
-    spec_verify_acceptance(_ptr(target), _ptr(draft), B, k, V, temperature, top_p, dt,
+    spec_verify_acceptance(_ptr(target), _ptr(draft), B, k, V, temperature, top_p, top_k, dt,
                            _ptr(out_beta), _ptr(out_tv), _ptr(workspace), workspace.numel(),
                            _stream(stream))
     return out_beta, out_tv

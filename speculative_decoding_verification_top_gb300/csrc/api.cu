@@ -76,7 +76,7 @@ struct ChainPlan {
     SeqArgs seq;
     Workspace ws;
     FinalArgs fin;
-    int stoch, dtype, rows_total, use_topp;
+    int stoch, dtype, rows_total, use_topp, top_k;
     float c, temperature, top_p;
     cudaStream_t st;
 };
@@ -87,7 +87,7 @@ int plan_chain(const void *target_logits, const void *draft_logits, const int32_
                const float *uniforms, int B, int k, int V, float temperature, float top_p,
                int mode, int dtype, int32_t *out_tokens, int32_t *out_num_accepted,
                void *workspace, size_t workspace_bytes, spec_stream_t stream, ChainPlan *plan,
-               bool qprob = false) {
+               bool qprob = false, int top_k = 0) {
     if (mode != SPEC_STOCHASTIC && mode != SPEC_GREEDY) return SPEC_ERR_MODE;
     if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_DTYPE;
     if (!chain_sizes_ok(B, k, V)) return SPEC_ERR_SHAPE;
@@ -110,7 +110,9 @@ int plan_chain(const void *target_logits, const void *draft_logits, const int32_
     plan->dtype = dtype;
     plan->temperature = stoch ? temperature : 1.0f;
     plan->top_p = stoch ? top_p : 1.0f;
-    plan->use_topp = stoch && top_p < 1.0f;
+    // top_k <= 0 or >= V keeps every logit (no top-k).
+    plan->top_k = stoch && top_k > 0 && top_k < V ? top_k : 0;
+    plan->use_topp = stoch && (top_p < 1.0f || plan->top_k > 0);
     plan->c = static_cast<float>(1.4426950408889634 / static_cast<double>(plan->temperature));
     plan->st = reinterpret_cast<cudaStream_t>(stream);
     carve(workspace, B, 2 * k + 1, V, &plan->ws, true);
@@ -142,7 +144,7 @@ int plan_chain(const void *target_logits, const void *draft_logits, const int32_
 
     SeqArgs &sq = plan->seq;
     sq.work = stoch ? kSeqDecide : kSeqGreedy;
-    sq.list_draw = stoch && top_p < 1.0f ? 1 : 0;
+    sq.list_draw = plan->use_topp ? 1 : 0;
     sq.qprob = qprob ? 1 : 0;
     sq.draft_tokens = draft_tokens;
     sq.uniforms = uniforms;
@@ -163,6 +165,7 @@ int launch_chain_rows(const ChainPlan &p) {
     ta.c = p.c;
     ta.temperature = p.temperature;
     ta.top_p = p.top_p;
+    ta.top_k = p.top_k;
     ta.ws = p.ws;
     return launch_topp_rows(ta, p.rows_total, p.dtype, p.st);
 }
@@ -215,6 +218,22 @@ SPEC_EXPORT int spec_verify_sample(const void *target_logits, const void *draft_
     return launch_chain_finish(plan);
 }
 
+SPEC_EXPORT int spec_verify_sample_topk(const void *target_logits, const void *draft_logits,
+                                        const int32_t *draft_tokens, const float *uniforms, int B,
+                                        int k, int V, float temperature, float top_p, int top_k,
+                                        int mode, int dtype, int32_t *out_tokens,
+                                        int32_t *out_num_accepted, void *workspace,
+                                        size_t workspace_bytes, spec_stream_t stream) {
+    ChainPlan plan;
+    int rc = plan_chain(target_logits, draft_logits, draft_tokens, uniforms, B, k, V, temperature,
+                        top_p, mode, dtype, out_tokens, out_num_accepted, workspace,
+                        workspace_bytes, stream, &plan, false, top_k);
+    if (rc != SPEC_OK || B == 0) return rc;
+    rc = launch_chain_rows(plan);
+    if (rc != SPEC_OK) return rc;
+    return launch_chain_finish(plan);
+}
+
 SPEC_EXPORT int spec_verify_sample_rows(const void *target_logits, const void *draft_logits,
                                         const int32_t *draft_tokens, const float *uniforms,
                                         int B, int k, int V, float temperature, float top_p,
@@ -246,13 +265,13 @@ SPEC_EXPORT int spec_verify_sample_finish(const void *target_logits, const void 
 SPEC_EXPORT int spec_verify_sample_probs(const void *target_logits, const float *draft_probs,
                                          const int32_t *draft_tokens, const float *uniforms,
                                          int B, int k, int V, float temperature, float top_p,
-                                         int dtype, int32_t *out_tokens,
+                                         int top_k, int dtype, int32_t *out_tokens,
                                          int32_t *out_num_accepted, void *workspace,
                                          size_t workspace_bytes, spec_stream_t stream) {
     ChainPlan plan;
     int rc = plan_chain(target_logits, draft_probs, draft_tokens, uniforms, B, k, V, temperature,
                         top_p, SPEC_STOCHASTIC, dtype, out_tokens, out_num_accepted, workspace,
-                        workspace_bytes, stream, &plan, true);
+                        workspace_bytes, stream, &plan, true, top_k);
     if (rc != SPEC_OK || B == 0) return rc;
     rc = launch_chain_rows(plan);
     if (rc != SPEC_OK) return rc;
@@ -355,7 +374,8 @@ SPEC_EXPORT int spec_verify_intermediates(const void *workspace, size_t workspac
 }
 
 SPEC_EXPORT int spec_verify_acceptance(const void *target_logits, const void *draft_logits, int B,
-                                       int k, int V, float temperature, float top_p, int dtype,
+                                       int k, int V, float temperature, float top_p, int top_k,
+                                       int dtype,
                                        float *out_beta, float *out_tv, void *workspace,
                                        size_t workspace_bytes, spec_stream_t stream) {
     if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_DTYPE;
@@ -383,7 +403,7 @@ SPEC_EXPORT int spec_verify_acceptance(const void *target_logits, const void *dr
     a.total = a.pairs * V;
     a.seg = 0;
     a.c = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
-    const bool masked = top_p < 1.0f;
+    const bool masked = top_p < 1.0f || (top_k > 0 && top_k < V);
     a.list = masked ? 1 : 0;
     a.beta = out_beta;
     a.tv = out_tv;

@@ -636,6 +636,7 @@ struct ToppArgs {
     RowView rows;
     SeqArgs seq;
     float c, temperature, top_p;
+    int top_k;         // keep the top_k largest logits and their ties first (0: off)
     Workspace ws;
 };
 

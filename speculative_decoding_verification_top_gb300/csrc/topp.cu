@@ -31,6 +31,10 @@
 //      narrowed from the row.)
 //   The row record gets lam and the kept mass; the warp that finishes a
 //   sequence's last row takes its accept decision.
+//   With top-k (a processor the target and the draft must share, "246
+//   Speculative Decoding", 6), the same select first runs by count: the
+//   K-th largest key, ties kept; top-p then runs on the kept set, its
+//   target top_p times the kept set's mass.
 
 #include "stream.cuh"
 
@@ -135,6 +139,7 @@ struct ToppShared {
     uint32_t cmax;                  // running max of the row so far (ordered key)
     int n_alist, n_elems, n_nuc;
     unsigned int kmin, kmax;
+    unsigned long long zacc;        // fixed-point mass of the top-k set
 };
 static_assert(sizeof(ToppShared) <= kToppSmem, "top-p shared memory");
 
@@ -393,7 +398,9 @@ __device__ __forceinline__ void stats_capture(ToppShared &sh, const T *rowp, int
     edge(sp.a1, sp.e1);
 }
 
-template <typename T>
+// TOPK: the top-k select is compiled in (its own instantiation, so that the
+// top-p-only kernel keeps its registers).
+template <typename T, bool TOPK>
 __global__ void __launch_bounds__(kTpThreads, 3) topp_kernel(const ToppArgs a) {
     // Let the dependent final-draw grid launch once every CTA of this grid
     // has started (it waits for this grid's completion before reading).
@@ -449,19 +456,11 @@ __global__ void __launch_bounds__(kTpThreads, 3) topp_kernel(const ToppArgs a) {
         const float c = a.c;
         const float negmc = -__fmul_rn(m, c);
         __syncthreads();
-        const unsigned long long tgt =
-            __float2ull_rn(__fmul_rn(__fmul_rn(a.top_p, Z), kFix));
-        const float c0 = m + a.temperature *
-                                 (logf((1.0f - a.top_p) * Z / static_cast<float>(V)) - 0.69314718f);
-        const float cut = fminf(c0, m);
-        // Pass A first over [y1, m]: y1 = m - kToppTry T, or c0 if higher.
-        // If the mass of the logits >= y1 already reaches top_p Z the
-        // crossing bin is found there (exactly: the histogram holds every
-        // logit >= y1); otherwise pass A runs again over [c0, m].
-        float lo = fmaxf(cut, m - tryT);
-        // The statistics pass kept every logit >= m - tryT (its floors never
-        // exceed that), so every logit >= lo, unless the list overflowed.
-        const bool from_list = sh.n_alist <= kAList;
+        // What the list holds: every logit >= list_lo (the statistics pass
+        // kept every logit >= m - tryT, unless the list overflowed).
+        const float tryfloor = m - tryT;
+        float list_lo = sh.n_alist <= kAList ? tryfloor : INFINITY;
+        uint32_t kfloor = 0u;  // keys below it are not kept (top-k; 0: none)
         float span = 0.0f, inv = 0.0f;
         auto vbin = [&](float l) {
             return min(static_cast<int>(__fmul_rn(__fsub_rn(m, l), inv)), kHistBins - 1);
@@ -469,103 +468,184 @@ __global__ void __launch_bounds__(kTpThreads, 3) topp_kernel(const ToppArgs a) {
         auto mass = [&](float l) {
             return __float2ull_rn(__fmul_rn(ex2(__fmaf_rn(l, c, negmc)), kFix));
         };
-        unsigned long long above = 0ull, hb = 0ull;
-        int b0 = 0;
-        for (int attempt = 0; attempt < 2; ++attempt) {
-            span = __fsub_rn(m, lo);
-            inv = span > 0.0f ? static_cast<float>(kHistBins) / span : 0.0f;
-            cta_clear(sh.sel);
-            if (attempt == 0 && from_list) {
-                const int na0 = sh.n_alist;
-                for (int i = tid; i < na0; i += kTpThreads) {
+        // One threshold select over the logits l >= lo with key >= kfloor,
+        // each weighing 1 (count) or its fixed-point mass: the largest key
+        // lam whose weight from the top reaches `target` (all ties of lam
+        // kept).  Pass A histograms the weight by value, uniformly over
+        // [lo, m], trying each lo of `los` in turn until the weight above it
+        // reaches target (the last one is final); from the list when it
+        // holds every logit >= lo, else from the row (refilling the list).
+        // Pass B gathers the crossing bin's logits and narrows by key to one.
+        // Sets sel_above / sel_hb (weight above lam / at lam, once narrowed
+        // to one key: sel_single) and sel_lo (the lo used).
+        unsigned long long sel_above = 0ull, sel_hb = 0ull;
+        float sel_lo = tryfloor;
+        bool sel_single = false;
+        auto select = [&](bool count, unsigned long long target, const float *los,
+                          int nlo) -> uint32_t {
+            auto wt = [&](float l) -> unsigned long long { return count ? 1ull : mass(l); };
+            float lo = los[0];
+            unsigned long long above = 0ull, hb = 0ull;
+            int b0 = 0;
+            for (int attempt = 0; attempt < nlo; ++attempt) {
+                lo = los[attempt];
+                span = __fsub_rn(m, lo);
+                inv = span > 0.0f ? static_cast<float>(kHistBins) / span : 0.0f;
+                cta_clear(sh.sel);
+                if (lo >= list_lo) {
+                    const int na0 = sh.n_alist;
+                    for (int i = tid; i < na0; i += kTpThreads) {
+                        const float l = sh.alist[i];
+                        if (l >= lo && okey<T>(l) >= kfloor)
+                            atomicAdd(&sh.sel.hist[vbin(l)], wt(l));
+                    }
+                } else {
+                    // From the row (it mostly hits L2), keeping every
+                    // logit >= lo in the list.
+                    if (tid == 0) sh.n_alist = 0;
+                    __syncthreads();
+                    for_row<T>(sh, rowp, V, lo, [&](float l, int x) {
+                        if (okey<T>(l) >= kfloor) atomicAdd(&sh.sel.hist[vbin(l)], wt(l));
+                        const int pos = atomicAdd(&sh.n_alist, 1);
+                        if (pos < kAList) {
+                            sh.alist[pos] = l;
+                            sh.aidx[pos] = x;
+                        }
+                    });
+                    __syncthreads();
+                    list_lo = sh.n_alist <= kAList ? lo : INFINITY;
+                }
+                __syncthreads();
+                bool crossed;
+                b0 = cta_cross(sh.sel, kHistBins, 0ull, target, &above, &hb, &crossed);
+                if (crossed) break;
+            }
+            // Pass B: the logits of bin b0 and their key range.  No logit
+            // below vmin can fall into b0 (the margin exceeds any rounding of
+            // vbin).
+            const float vlo =
+                b0 == kHistBins - 1
+                    ? lo
+                    : __fsub_rn(m, __fmul_rn(static_cast<float>(b0 + 1), span / kHistBins));
+            const float vmin =
+                fmaxf(lo, vlo - span * 9.5367431640625e-7f - fabsf(vlo) * 9.5367431640625e-7f);
+            if (tid == 0) {
+                sh.n_elems = 0;
+                sh.kmin = 0xFFFFFFFFu;
+                sh.kmax = 0u;
+            }
+            __syncthreads();
+            auto in_b0 = [&](float l) {
+                return l >= lo && okey<T>(l) >= kfloor && vbin(l) == b0;
+            };
+            auto take = [&](float l, int) {
+                if (in_b0(l)) {
+                    const int pos = atomicAdd(&sh.n_elems, 1);
+                    if (pos < kElemCap) sh.elems[pos] = l;
+                    atomicMin(&sh.kmin, okey<T>(l));
+                    atomicMax(&sh.kmax, okey<T>(l));
+                }
+            };
+            if (lo >= list_lo) {
+                const int na = sh.n_alist;
+                for (int i = tid; i < na; i += kTpThreads) take(sh.alist[i], 0);
+            } else {
+                for_row<T>(sh, rowp, V, vmin, take);
+            }
+            __syncthreads();
+            const int ne = sh.n_elems;
+            uint32_t klo = sh.kmin, khi = sh.kmax;
+            // Narrow by key inside bin b0.
+            for (int pass = 0; pass < 4 && khi > klo; ++pass) {
+                const unsigned long long W = static_cast<unsigned long long>(khi - klo) + 1ull;
+                const int nb = W < static_cast<unsigned long long>(kHistBins) ? static_cast<int>(W)
+                                                                               : kHistBins;
+                cta_clear(sh.sel);
+                auto add = [&](float l) {
+                    const uint32_t key = okey<T>(l);
+                    if (key < klo || key > khi) return;
+                    const int bin =
+                        static_cast<int>((static_cast<unsigned long long>(khi - key) * nb) / W);
+                    atomicAdd(&sh.sel.hist[bin], wt(l));
+                };
+                if (ne <= kElemCap) {
+                    for (int i = tid; i < ne; i += kTpThreads) add(sh.elems[i]);
+                } else {
+                    for_row<T>(sh, rowp, V, vmin, [&](float l, int) {
+                        if (in_b0(l)) add(l);
+                    });
+                }
+                __syncthreads();
+                bool cr;
+                unsigned long long ab;
+                const int b = cta_cross(sh.sel, nb, above, target, &ab, &hb, &cr);
+                above = ab;
+                const unsigned long long lo_off =
+                    (static_cast<unsigned long long>(b) * W + nb - 1) / nb;
+                const unsigned long long hi_off =
+                    (static_cast<unsigned long long>(b + 1) * W + nb - 1) / nb - 1;
+                const uint32_t nkhi = khi - static_cast<uint32_t>(lo_off);
+                klo = khi - static_cast<uint32_t>(hi_off);
+                khi = nkhi;
+            }
+            sel_above = above;
+            sel_hb = hb;
+            sel_lo = lo;
+            sel_single = khi == klo;
+            return khi;
+        };
+        float zsel = Z;          // mass the top-p target is relative to
+        float final_lo = tryfloor;  // every kept logit is >= it
+        bool have_lam = false;
+        if (TOPK && a.top_k > 0 && a.top_k < V) {
+            // Top-k: the K-th largest key by count, over the logits near
+            // the max first (the list), then over ever wider windows of the
+            // row; beyond the widest (4608 T below the max) a logit's
+            // weight 2^((l - m) c) is zero in fp32.
+            const float los[4] = {tryfloor, m - 8.0f * tryT, m - 64.0f * tryT, m - 512.0f * tryT};
+            const uint32_t tau = select(true, static_cast<unsigned long long>(a.top_k), los, 4);
+            const float lo_k = sel_lo;
+            kfloor = tau;
+            // Fixed-point mass of the kept set (keys >= tau, all >= lo_k).
+            if (tid == 0) sh.zacc = 0ull;
+            __syncthreads();
+            if (lo_k >= list_lo) {
+                const int na = sh.n_alist;
+                for (int i = tid; i < na; i += kTpThreads) {
                     const float l = sh.alist[i];
-                    if (l >= lo) atomicAdd(&sh.sel.hist[vbin(l)], mass(l));
+                    if (okey<T>(l) >= tau) atomicAdd(&sh.zacc, mass(l));
                 }
             } else {
-                // From the row: pass A again (it mostly hits L2), keeping
-                // the logits >= lo.
-                if (tid == 0) sh.n_alist = 0;
-                __syncthreads();
-                for_row<T>(sh, rowp, V, lo, [&](float l, int x) {
-                    atomicAdd(&sh.sel.hist[vbin(l)], mass(l));
-                    const int pos = atomicAdd(&sh.n_alist, 1);
-                    if (pos < kAList) {
-                        sh.alist[pos] = l;
-                        sh.aidx[pos] = x;
-                    }
+                for_row<T>(sh, rowp, V, lo_k, [&](float l, int) {
+                    if (okey<T>(l) >= tau) atomicAdd(&sh.zacc, mass(l));
                 });
             }
             __syncthreads();
-            bool crossed;
-            b0 = cta_cross(sh.sel, kHistBins, 0ull, tgt, &above, &hb, &crossed);
-            if (crossed || lo == cut) break;
-            lo = cut;
-        }
-        // Pass B: the logits of bin b0 and their key range.  No logit below
-        // vmin can fall into b0 (the margin exceeds any rounding of vbin).
-        const float vlo =
-            b0 == kHistBins - 1
-                ? lo
-                : __fsub_rn(m, __fmul_rn(static_cast<float>(b0 + 1), span / kHistBins));
-        const float vmin =
-            fmaxf(lo, vlo - span * 9.5367431640625e-7f - fabsf(vlo) * 9.5367431640625e-7f);
-        if (tid == 0) {
-            sh.n_elems = 0;
-            sh.kmin = 0xFFFFFFFFu;
-            sh.kmax = 0u;
-        }
-        __syncthreads();
-        const int na = sh.n_alist;
-        auto take = [&](float l, int) {
-            if (l >= lo && vbin(l) == b0) {
-                const int pos = atomicAdd(&sh.n_elems, 1);
-                if (pos < kElemCap) sh.elems[pos] = l;
-                atomicMin(&sh.kmin, okey<T>(l));
-                atomicMax(&sh.kmax, okey<T>(l));
+            zsel = __fmul_rn(__ull2float_rn(sh.zacc), 1.0f / kFix);
+            final_lo = lo_k;
+            if (!(a.top_p < 1.0f)) {
+                lam = tau;
+                zk = zsel;
+                have_lam = true;
             }
-        };
-        if (na <= kAList) {
-            for (int i = tid; i < na; i += kTpThreads) take(sh.alist[i], 0);
-        } else {
-            for_row<T>(sh, rowp, V, vmin, take);
         }
-        __syncthreads();
-        const int ne = sh.n_elems;
-        uint32_t klo = sh.kmin, khi = sh.kmax;
-        // Narrow by key inside bin b0.
-        for (int pass = 0; pass < 4 && khi > klo; ++pass) {
-            const unsigned long long W = static_cast<unsigned long long>(khi - klo) + 1ull;
-            const int nb = W < static_cast<unsigned long long>(kHistBins) ? static_cast<int>(W)
-                                                                           : kHistBins;
-            cta_clear(sh.sel);
-            auto add = [&](float l) {
-                const uint32_t key = okey<T>(l);
-                if (key < klo || key > khi) return;
-                const int bin =
-                    static_cast<int>((static_cast<unsigned long long>(khi - key) * nb) / W);
-                atomicAdd(&sh.sel.hist[bin], mass(l));
-            };
-            if (ne <= kElemCap) {
-                for (int i = tid; i < ne; i += kTpThreads) add(sh.elems[i]);
-            } else {
-                for_row<T>(sh, rowp, V, vmin, [&](float l, int) {
-                    if (l >= lo && vbin(l) == b0) add(l);
-                });
-            }
-            __syncthreads();
-            bool cr;
-            unsigned long long ab;
-            const int b = cta_cross(sh.sel, nb, above, tgt, &ab, &hb, &cr);
-            above = ab;
-            const unsigned long long lo_off = (static_cast<unsigned long long>(b) * W + nb - 1) / nb;
-            const unsigned long long hi_off =
-                (static_cast<unsigned long long>(b + 1) * W + nb - 1) / nb - 1;
-            const uint32_t nkhi = khi - static_cast<uint32_t>(lo_off);
-            klo = khi - static_cast<uint32_t>(hi_off);
-            khi = nkhi;
+        if (!have_lam) {
+            // Top-p over the kept set: the target is top_p of its mass.
+            // Logits below c0 = m + T (ln((1 - top_p) zsel / V) - ln 2)
+            // cannot be in the nucleus: all of them carry < (1 - top_p) zsel
+            // / 2.  Pass A first tries max(c0, m - tryT) (a nucleus usually
+            // ends far above c0), then c0.
+            const unsigned long long tgt =
+                __float2ull_rn(__fmul_rn(__fmul_rn(a.top_p, zsel), kFix));
+            const float c0 =
+                m + a.temperature *
+                        (logf((1.0f - a.top_p) * zsel / static_cast<float>(V)) - 0.69314718f);
+            const float cut = fminf(c0, m);
+            const float los[2] = {fmaxf(cut, tryfloor), cut};
+            lam = select(false, tgt, los, los[0] == cut ? 1 : 2);
+            zk = __fmul_rn(__ull2float_rn(sel_single ? sel_above + sel_hb : tgt), 1.0f / kFix);
+            final_lo = sel_lo;
         }
-        lam = khi;
-        zk = __fmul_rn(__ull2float_rn(khi == klo ? above + hb : tgt), 1.0f / kFix);
         // The nucleus list of a target row for the final draw: the kept
         // logits (keys >= lam, all of them >= lo, so all in pass A's list
         // when it did not overflow), ranked by index, each with the draft
@@ -577,7 +657,9 @@ __global__ void __launch_bounds__(kTpThreads, 3) topp_kernel(const ToppArgs a) {
             if (tid == 0) sh.n_nuc = 0;
             __syncthreads();
             const int na2 = sh.n_alist;
-            if (na2 <= kAList) {
+            // The list holds every kept logit (all are >= final_lo).
+            const bool covers = na2 <= kAList && final_lo >= list_lo;
+            if (covers) {
                 for (int i = tid; i < na2; i += kTpThreads)
                     if (okey<T>(sh.alist[i]) >= lam) {
                         const int pos = atomicAdd(&sh.n_nuc, 1);
@@ -589,7 +671,7 @@ __global__ void __launch_bounds__(kTpThreads, 3) topp_kernel(const ToppArgs a) {
             }
             __syncthreads();
             const int nn = sh.n_nuc;
-            const bool ok = na2 <= kAList && nn <= min(kElemCap, kNucCap);
+            const bool ok = covers && nn <= min(kElemCap, kNucCap);
             const int tr = bq * (kk + 1) + rq;
             uint4 *L = a.ws.nuc + static_cast<size_t>(tr) * kNucCap;
             // The draft value at each index: a logit, or (draft given as
@@ -687,7 +769,7 @@ __global__ void __launch_bounds__(kTpThreads, 3) topp_kernel(const ToppArgs a) {
 template <typename K>
 bool topp_smem_ok(K kernel, int slot) {
     constexpr int kMaxDev = 64;
-    static int done[kMaxDev][2];
+    static int done[kMaxDev][4];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return false;
     if (__atomic_load_n(&done[dev][slot], __ATOMIC_RELAXED)) return true;
@@ -698,20 +780,28 @@ bool topp_smem_ok(K kernel, int slot) {
     return true;
 }
 
-}  // namespace
-
-int launch_topp_rows(const ToppArgs &a, int rows_total, int dtype, cudaStream_t st) {
-    const bool ok = dtype == SPEC_F32 ? topp_smem_ok(topp_kernel<float>, 0)
-                                      : topp_smem_ok(topp_kernel<uint16_t>, 1);
-    if (!ok) return SPEC_ERR_CUDA;
+template <typename T, bool TOPK>
+int launch_topp_t(const ToppArgs &a, int rows_total, cudaStream_t st) {
+    if (!topp_smem_ok(topp_kernel<T, TOPK>, (sizeof(T) == 2 ? 1 : 0) + (TOPK ? 2 : 0)))
+        return SPEC_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(rows_total));
     cfg.blockDim = dim3(kTpThreads);
     cfg.dynamicSmemBytes = kToppSmem;
     cfg.stream = st;  // first kernel of a call: plain stream order
-    const cudaError_t e = dtype == SPEC_F32 ? cudaLaunchKernelEx(&cfg, topp_kernel<float>, a)
-                                            : cudaLaunchKernelEx(&cfg, topp_kernel<uint16_t>, a);
-    return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+    return cudaLaunchKernelEx(&cfg, topp_kernel<T, TOPK>, a) == cudaSuccess ? SPEC_OK
+                                                                             : SPEC_ERR_CUDA;
+}
+
+}  // namespace
+
+int launch_topp_rows(const ToppArgs &a, int rows_total, int dtype, cudaStream_t st) {
+    const bool topk = a.top_k > 0;
+    if (dtype == SPEC_F32)
+        return topk ? launch_topp_t<float, true>(a, rows_total, st)
+                    : launch_topp_t<float, false>(a, rows_total, st);
+    return topk ? launch_topp_t<uint16_t, true>(a, rows_total, st)
+                : launch_topp_t<uint16_t, false>(a, rows_total, st);
 }
 
 }  // namespace specv

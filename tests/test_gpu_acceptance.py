@@ -172,10 +172,10 @@ def test_argument_errors():
     _, _, ws = sv.verify_sample(tg, dr, dev(wl.draft_tokens), dev(wl.uniforms))
     out = torch.empty((2, 2), dtype=torch.float32, device=DEV)
     with pytest.raises(sv.SpecVerifyError):
-        sv.spec_verify_acceptance(tg.data_ptr(), dr.data_ptr(), 2, 2, 64, 0.0, 1.0, sv.SPEC_F32,
+        sv.spec_verify_acceptance(tg.data_ptr(), dr.data_ptr(), 2, 2, 64, 0.0, 1.0, 0, sv.SPEC_F32,
                                   out.data_ptr(), None, ws.data_ptr(), ws.numel())
     with pytest.raises(sv.SpecVerifyError):
-        sv.spec_verify_acceptance(tg.data_ptr(), dr.data_ptr(), 2, 2, 64, 1.0, 1.0, sv.SPEC_F32,
+        sv.spec_verify_acceptance(tg.data_ptr(), dr.data_ptr(), 2, 2, 64, 1.0, 1.0, 0, sv.SPEC_F32,
                                   out.data_ptr(), None, ws.data_ptr(), 16)
-    assert sv.spec_verify_acceptance(None, None, 0, 2, 64, 1.0, 1.0, sv.SPEC_F32, None, None,
+    assert sv.spec_verify_acceptance(None, None, 0, 2, 64, 1.0, 1.0, 0, sv.SPEC_F32, None, None,
                                      None, 0) == 0

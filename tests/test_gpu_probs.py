@@ -152,7 +152,7 @@ def test_argument_errors():
     ws = sv.new_workspace(sv.spec_verify_workspace_size(2, 2, 64), DEV)
     out_t = torch.empty((2, 3), dtype=torch.int32, device=DEV)
     out_n = torch.empty((2,), dtype=torch.int32, device=DEV)
-    args = [tg.data_ptr(), qd.data_ptr(), tk.data_ptr(), un.data_ptr(), 2, 2, 64, 1.0, 1.0,
+    args = [tg.data_ptr(), qd.data_ptr(), tk.data_ptr(), un.data_ptr(), 2, 2, 64, 1.0, 1.0, 0,
             sv.SPEC_F32, out_t.data_ptr(), out_n.data_ptr(), ws.data_ptr(), ws.numel()]
     bad = list(args)
     bad[1] = qd.data_ptr() + 2  # not 4-byte aligned
