@@ -407,6 +407,28 @@ def timed_tree_mask(job, launches=200):
     return out
 
 
+def timed_topk(job, K=50, launches=200):
+    """spec_verify_sample_topk with top-k K on the workload (and its top-p):
+    device time per call over the same logits."""
+    import torch
+    wl, sv = job.wl, job.sv
+
+    def one(i):
+        a = job.chain_args(i)
+        sv.spec_verify_sample_topk(*a[:9], K, *a[9:])
+
+    for i in range(3):
+        one(i)
+    torch.cuda.synchronize()
+    ms = device_launch_ms(one, launches, job.stream)
+    nbytes = wl.logit_bytes()
+    job.step(0)  # leave the workspace as a plain call left it
+    torch.cuda.synchronize()
+    return {"entry": "spec_verify_sample_topk", "top_k": K, "top_p": wl.top_p,
+            "launches": launches, "avg_call_us": round(ms * 1e3, 2), "bytes": nbytes,
+            "achieved_gbs": round(nbytes / (ms * 1e-3) / 1e9, 1)}
+
+
 def timed_e2e(job, steps):
     """Host buffers -> device -> library call -> results back to the host."""
     import torch
@@ -497,6 +519,7 @@ def run_ours(args):
     clk = clocks.stop()
     accept = timed_acceptance(job) if mode != "tree" else None
     probs = timed_probs(job) if mode != "tree" else None
+    topk = timed_topk(job) if mode != "tree" else None
     tmask = timed_tree_mask(job) if mode == "tree" else None
     total_ms = max_over_ranks(total_ms, world)
 
@@ -553,6 +576,9 @@ def run_ours(args):
         out["acceptance"] = accept
     if tmask is not None:
         out["tree_mask"] = tmask
+    if topk is not None:
+        topk["frac"] = round(topk["achieved_gbs"] / peak, 4)
+        out["top_k"] = topk
     if probs is not None:
         probs["frac"] = round(probs["achieved_gbs"] / peak, 4)
         out["draft_probs"] = probs
