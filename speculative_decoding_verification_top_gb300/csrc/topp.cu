@@ -386,7 +386,8 @@ __device__ __forceinline__ void stats_capture(ToppShared &sh, const T *rowp, int
         // finite floor excludes -inf logits; with no finite max yet the
         // floor is +inf.)
         uint32_t mask = 0u;
-        if (bm >= thr) {
+        // Once the list has overflowed it is not used: stop filling it.
+        if (bm >= thr && *reinterpret_cast<volatile int *>(&sh.n_alist) <= kAList) {
 #pragma unroll
             for (int i = 0; i < kBatch * P; ++i)
                 if (h[i] >= thr) mask |= 1u << i;
@@ -599,11 +600,28 @@ __global__ void __launch_bounds__(kTpThreads, 3) topp_kernel(const ToppArgs a) {
         bool have_lam = false;
         if (TOPK && a.top_k > 0 && a.top_k < V) {
             // Top-k: the K-th largest key by count, over the logits near
-            // the max first (the list), then over ever wider windows of the
-            // row; beyond the widest (4608 T below the max) a logit's
-            // weight 2^((l - m) c) is zero in fp32.
-            const float los[4] = {tryfloor, m - 8.0f * tryT, m - 64.0f * tryT, m - 512.0f * tryT};
-            const uint32_t tau = select(true, static_cast<unsigned long long>(a.top_k), los, 4);
+            // the max first (the list), then over windows of the row 1.5
+            // times wider each (a window that first holds K logits then holds
+            // few more, so they mostly fit the list for the passes after);
+            // beyond the widest (4608 T below the max) a logit's weight
+            // 2^((l - m) c) is zero in fp32.
+            // If the list overflowed, the row is dense near its max and the
+            // K-th largest usually lies well inside tryT: the windows start
+            // at tryT / 4 (from the row) and double up to tryT first.
+            float los[11];
+            int nlo = 0;
+            if (list_lo == INFINITY) {
+                los[nlo++] = __fsub_rn(m, __fmul_rn(0.25f, tryT));
+                los[nlo++] = __fsub_rn(m, __fmul_rn(0.5f, tryT));
+            }
+            los[nlo++] = tryfloor;
+            float wdt = tryT;
+            for (int i = 0; i < 7; ++i) {
+                wdt = __fmul_rn(wdt, 1.5f);
+                los[nlo++] = __fsub_rn(m, wdt);
+            }
+            los[nlo++] = __fsub_rn(m, __fmul_rn(512.0f, tryT));
+            const uint32_t tau = select(true, static_cast<unsigned long long>(a.top_k), los, nlo);
             const float lo_k = sel_lo;
             kfloor = tau;
             // Fixed-point mass of the kept set (keys >= tau, all >= lo_k).
