@@ -87,6 +87,8 @@ def _load():
         lib.oracle_tree_mask.restype = I
         lib.oracle_ancestor_mask.argtypes = [P, I, P]
         lib.oracle_ancestor_mask.restype = I
+        lib.oracle_verify_tree_sample.argtypes = [P, P, I, P, P, P, I, I, I, I, D, D, I, P, P, P, P]
+        lib.oracle_verify_tree_sample.restype = I
         lib.oracle_verify_tree.argtypes = [P, I, P, P, I, I, I, I, P, P, P]
         lib.oracle_verify_tree.restype = I
         _lib = lib
@@ -291,3 +293,31 @@ def boundary_flags(res, uniforms, top_p=1.0, tol=1e-5):
         near = (np.abs(info[:, :, 2] - top_p) < tol) | (np.abs(info[:, :, 3] - top_p) < tol)
         flag |= np.any(near, axis=1)
     return flag & (j >= 0)
+
+
+def verify_tree_sample(target, draft, parents, node_tokens, uniforms, depth, T=1.0, top_p=1.0,
+                       top_k=0):
+    """Stochastic tree verification (reading R11).  target, draft [B, N, V];
+    parents [N]; node_tokens [B, N]; uniforms [B, N] (entry 0: the final
+    draw, entry c: node c's test).  Returns dict(tokens [B, D+1],
+    num_accepted [B], path [B, D+1], margin [B], errors)."""
+    tgt, dt = _logits(target)
+    drf, dt2 = _logits(draft)
+    B, N, V = tgt.shape
+    if dt2 != dt or drf.shape != (B, N, V):
+        raise ValueError("draft logits must match target dtype and be [B, N, V]")
+    par = np.ascontiguousarray(parents, np.int32)
+    tok = np.ascontiguousarray(node_tokens, np.int32).reshape(B, N)
+    uni = np.ascontiguousarray(uniforms, np.float32).reshape(B, N)
+    W = depth + 1
+    out_t = np.zeros((B, W), np.int32)
+    out_n = np.zeros(B, np.int32)
+    out_p = np.zeros((B, W), np.int32)
+    mg = np.zeros(B, np.float64)
+    err = _load().oracle_verify_tree_sample(_ptr(tgt), _ptr(drf), dt, _ptr(par), _ptr(tok),
+                                            _ptr(uni), B, N, V, int(depth), float(T),
+                                            float(top_p), int(top_k), _ptr(out_t), _ptr(out_n),
+                                            _ptr(out_p), _ptr(mg))
+    if err < 0:
+        raise ValueError("oracle_verify_tree_sample rejected its arguments")
+    return dict(tokens=out_t, num_accepted=out_n, path=out_p, margin=mg, errors=err)

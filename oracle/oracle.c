@@ -52,6 +52,13 @@
  *      K-th kept, as in R1), renormalise; applied after temperature (which
  *      does not change the order) and before top-p, which then runs on the
  *      renormalised top-k distribution.  K <= 0 or K >= V: no top-k.
+ *   R11 stochastic tree ([LZ] "Tree verification" names SpecInfer's
+ *      lossless multi-candidate acceptance rule for sampling without
+ *      stating it): the children of a node are candidates drawn
+ *      independently from the draft row of that node; they are tried in
+ *      flattened order against a target that becomes the normalised
+ *      residual max(0, p' - q) after each rejected child (see
+ *      oracle_verify_tree_sample).
  *   R8 draft given as probabilities: the step takes the draft "logits (or
  *      probabilities)".  Reading: a probability row is q itself, the
  *      distribution the drafter sampled from -- used as given (no
@@ -750,5 +757,137 @@ int oracle_verify_tree(const void *target, int dtype, const int32_t *parents,
     free(g);
     free(acc);
     free(path);
+    return errors;
+}
+
+/*
+ * Stochastic tree verification, reading R11.  [LZ] "Tree verification"
+ * names SpecInfer's lossless multi-candidate acceptance rule for sampling
+ * without stating it.  Reading: the children of node n are candidates
+ * drawn independently from q_n (draft row n).  At the current node the
+ * children are tried in flattened order; child c is accepted iff
+ *   u_c * q_n(x_c) < p'(x_c)
+ * where p' starts as p_n (target row n) and, after each rejected child,
+ * becomes the residual max(0, p' - q_n) normalised (kept when that residual
+ * is zero everywhere, R4).  An accepted child becomes the current node; when
+ * every child is rejected, or the node has none, the final token is drawn
+ * from p' by inverse CDF (R3) with the final uniform.  Each try is the
+ * one-token rule against target p', so every emitted position follows p.
+ *
+ * target [B, N, V], draft [B, N, V] (row n: the law node n's children were
+ * drawn from), parents [N] (as oracle_verify_tree), node_tokens [B, N],
+ * uniforms [B, N]: entry c >= 1 for node c's test, entry 0 for the final
+ * draw.  T, top_p, top_k process target and draft rows alike.
+ * out_tokens [B, D+1] (path tokens, drawn token, -1), out_num [B] (depth,
+ * -1 on a data error), out_path [B, D+1] (optional),
+ * margin [B] (optional): the smallest distance of a uniform used to its
+ * decision boundary (|u - p'/q| over the tests run with q > 0, |u - C/S| at
+ * the drawn token's two CDF edges).
+ */
+int oracle_verify_tree_sample(const void *target, const void *draft, int dtype,
+                              const int32_t *parents, const int32_t *node_tokens,
+                              const float *uniforms, int B, int N, int V, int D,
+                              double T, double top_p, int top_k, int32_t *out_tokens,
+                              int32_t *out_num, int32_t *out_path, double *margin)
+{
+    if (!target || !draft || !parents || !node_tokens || !uniforms || !out_tokens ||
+        !out_num || B < 0 || N < 1 || V < 1 || D < 0 ||
+        (dtype != ORC_F32 && dtype != ORC_BF16) || !(T > 0.0) || !(top_p > 0.0) ||
+        top_p > 1.0)
+        return ORC_BAD_ARGUMENT;
+    const size_t esz = dtype == ORC_F32 ? 4 : 2;
+    const int W = D + 1;
+    int32_t *depth = (int32_t *)malloc((size_t)N * sizeof *depth);
+    int32_t *path = (int32_t *)malloc((size_t)W * sizeof *path);
+    double *p = (double *)malloc((size_t)N * V * sizeof *p);
+    double *q = (double *)malloc((size_t)N * V * sizeof *q);
+    double *pr = (double *)malloc((size_t)V * sizeof *pr);
+    int errors = 0;
+
+    int shape = tree_depths(parents, N, depth);
+    for (int n = 0; n < N && shape == ORC_OK; ++n)
+        if (depth[n] > D) shape = ORC_TREE_SHAPE;
+
+    for (int b = 0; b < B; ++b) {
+        int32_t *ot = out_tokens + (size_t)b * W;
+        int32_t *op = out_path ? out_path + (size_t)b * W : NULL;
+        const int32_t *tok = node_tokens + (size_t)b * N;
+        const float *ub = uniforms + (size_t)b * N;
+        int bad = shape != ORC_OK ? 1 << shape : 0;
+        for (int n = 1; n < N; ++n)
+            if (tok[n] < 0 || tok[n] >= V) bad |= 1 << ORC_TOKEN_RANGE;
+        for (int n = 0; n < N; ++n)
+            if (!(ub[n] >= 0.0f && ub[n] < 1.0f)) bad |= 1 << ORC_UNIFORM_RANGE;
+        for (int n = 0; n < N; ++n) {
+            const char *trow = (const char *)target + ((size_t)b * N + n) * V * esz;
+            const char *drow = (const char *)draft + ((size_t)b * N + n) * V * esz;
+            int s1 = oracle_process_row_k(trow, dtype, V, T, top_p, top_k, p + (size_t)n * V, NULL);
+            int s2 = oracle_process_row_k(drow, dtype, V, T, top_p, top_k, q + (size_t)n * V, NULL);
+            if (s1 != ORC_OK) bad |= 1 << s1;
+            if (s2 != ORC_OK) bad |= 1 << s2;
+        }
+        if (margin) margin[b] = INFINITY;
+        if (bad) {
+            errors |= bad;
+            fail_sequence(ot, W, &out_num[b]);
+            if (op)
+                for (int i = 0; i < W; ++i) op[i] = -1;
+            continue;
+        }
+
+        double mg = INFINITY;
+        int cur = 0, d = 0;
+        path[0] = 0;
+        int32_t drawn = -1;
+        for (;;) {
+            const double *qn = q + (size_t)cur * V;
+            memcpy(pr, p + (size_t)cur * V, (size_t)V * sizeof *pr);
+            int next = -1;
+            for (int c = 1; c < N && next < 0; ++c) {
+                if (parents[c] != cur) continue;
+                const double P = pr[tok[c]], Q = qn[tok[c]];
+                if (Q > 0.0 && fabs((double)ub[c] - P / Q) < mg) mg = fabs((double)ub[c] - P / Q);
+                if ((double)ub[c] * Q < P) {
+                    next = c;
+                    break;
+                }
+                double S = 0.0;
+                for (int x = 0; x < V; ++x) {
+                    double r = pr[x] - qn[x];
+                    S += r > 0.0 ? r : 0.0;
+                }
+                if (S > 0.0)
+                    for (int x = 0; x < V; ++x) {
+                        double r = pr[x] - qn[x];
+                        pr[x] = r > 0.0 ? r / S : 0.0;
+                    }
+            }
+            if (next < 0) {
+                double edges[3];
+                drawn = oracle_inverse_cdf(pr, V, (double)ub[0], edges);
+                double e0 = fabs((double)ub[0] - edges[1] / edges[0]);
+                double e1 = fabs((double)ub[0] - edges[2] / edges[0]);
+                if (e0 < mg) mg = e0;
+                if (e1 < mg) mg = e1;
+                break;
+            }
+            cur = next;
+            path[++d] = next;
+        }
+        for (int i = 0; i < W; ++i) ot[i] = -1;
+        for (int i = 0; i < d; ++i) ot[i] = tok[path[i + 1]];
+        ot[d] = drawn;
+        if (op) {
+            for (int i = 0; i < W; ++i) op[i] = -1;
+            for (int i = 0; i <= d; ++i) op[i] = path[i];
+        }
+        out_num[b] = d;
+        if (margin) margin[b] = mg;
+    }
+    free(depth);
+    free(path);
+    free(p);
+    free(q);
+    free(pr);
     return errors;
 }
