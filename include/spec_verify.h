@@ -257,6 +257,48 @@ int spec_verify_tree(const void *target_logits, const int32_t *parents,
                      spec_stream_t stream);
 
 /*
+ * Stochastic tree verification for B sequences sharing one tree shape --
+ * [LZ] "Tree verification" names SpecInfer's lossless multi-candidate
+ * acceptance rule for sampling, without stating it.  Reading: the children
+ * of node n are candidates drawn independently from q_n (draft row n,
+ * processed like the target).  From the root, the current node's children
+ * are tried in flattened order: child c is accepted iff
+ *   u_c * q_n(x_c) < p'(x_c)
+ * where p' starts as p_n (target row n) and becomes, after each rejected
+ * child, the residual max(0, p' - q_n) normalised (kept as it is if that
+ * residual is zero everywhere).  An accepted child becomes the current
+ * node; when every child is rejected, or there is none, the final token is
+ * drawn from p' by inverse CDF in token order.  Every emitted position
+ * then follows the target's distribution.
+ *
+ * Arguments
+ *   target_logits    [B, N, V] dtype, device: target row of each node
+ *   draft_logits     [B, N, V] dtype, device: row n is the law the children
+ *                    of node n were drawn from (a leaf's row is not used)
+ *   parents          [N] int32, device (as spec_verify_tree); at most 64
+ *                    children per node
+ *   node_tokens      [B, N] int32, device (the root's entry is ignored)
+ *   uniforms         [B, N] fp32 in [0, 1), device: entry c >= 1 is node
+ *                    c's test, entry 0 the final draw
+ *   1 <= N <= SPEC_MAX_TREE_NODES, 0 <= D < N; temperature, top_p, top_k
+ *                    process target and draft rows alike (as
+ *                    spec_verify_sample_topk)
+ *   out_tokens, out_num_accepted, out_path: as spec_verify_tree
+ *   workspace        >= spec_verify_tree_sample_workspace_size(B, N, V)
+ * Data errors: as spec_verify_tree, plus a uniform outside [0, 1) and a node
+ * with more than 64 children (SPEC_DATA_TREE_SHAPE).
+ * Returns SPEC_OK or a negative status.
+ */
+int spec_verify_tree_sample_workspace_size(int B, int N, int V, size_t *bytes);
+int spec_verify_tree_sample(const void *target_logits, const void *draft_logits,
+                            const int32_t *parents, const int32_t *node_tokens,
+                            const float *uniforms, int B, int N, int V, int D,
+                            float temperature, float top_p, int top_k, int dtype,
+                            int32_t *out_tokens, int32_t *out_num_accepted,
+                            int32_t *out_path, void *workspace, size_t workspace_bytes,
+                            spec_stream_t stream);
+
+/*
  * Tree attention inputs for B candidate trees -- the step just before the
  * target pass whose logits spec_verify_tree verifies.  [LZ] "Tree
  * verification": the flattened tree is scored in one target pass where

@@ -29,7 +29,7 @@ LIB_PATH = os.path.join(_PKG, "libspecverify.so")
 CSRC = os.path.join(_PKG, "csrc")
 SOURCES = [os.path.join(CSRC, f)
            for f in ("api.cu", "rows.cu", "topp.cu", "final.cu", "noalloc.cu",
-                     "accept.cu", "treemask.cu")]
+                     "accept.cu", "treemask.cu", "treesample.cu")]
 HEADERS = [os.path.join(CSRC, f) for f in ("common.cuh", "stream.cuh", "draw.cuh")]
 INCLUDE = os.path.join(_ROOT, "include")
 HEADER = os.path.join(INCLUDE, "spec_verify.h")
@@ -61,6 +61,8 @@ EXPORTED = (
     "spec_verify_acceptance",
     "spec_verify_sample_probs",
     "spec_verify_tree_mask",
+    "spec_verify_tree_sample_workspace_size",
+    "spec_verify_tree_sample",
     "spec_verify_status_string",
 )
 
@@ -125,6 +127,9 @@ def lib():
         L.spec_verify_acceptance.argtypes = [P, P, I, I, I, F, F, I, I, P, P, P, Z, P]
         L.spec_verify_sample_probs.argtypes = [P, P, P, P, I, I, I, F, F, I, I, P, P, P, Z, P]
         L.spec_verify_tree_mask.argtypes = [P, P, I, I, P, P, P, P]
+        L.spec_verify_tree_sample_workspace_size.argtypes = [I, I, I, ctypes.POINTER(Z)]
+        L.spec_verify_tree_sample.argtypes = [P, P, P, P, P, I, I, I, I, F, F, I, I, P, P, P, P,
+                                              Z, P]
         L.spec_verify_status_string.argtypes = [I]
         L.spec_verify_status_string.restype = ctypes.c_char_p
         for name in EXPORTED[:-1]:
@@ -242,6 +247,21 @@ def spec_verify_tree_mask(parents_ptr, pos0_ptr, B, N, out_mask_ptr, out_bias_pt
                           stream=0):
     return _check(lib().spec_verify_tree_mask(parents_ptr, pos0_ptr, B, N, out_mask_ptr,
                                               out_bias_ptr, out_pos_ptr, stream))
+
+
+def spec_verify_tree_sample_workspace_size(B, N, V):
+    out = ctypes.c_size_t(0)
+    _check(lib().spec_verify_tree_sample_workspace_size(B, N, V, ctypes.byref(out)))
+    return out.value
+
+
+def spec_verify_tree_sample(target_ptr, draft_ptr, parents_ptr, node_tokens_ptr, uniforms_ptr,
+                            B, N, V, D, temperature, top_p, top_k, dtype, out_tokens_ptr,
+                            out_num_ptr, out_path_ptr, workspace_ptr, workspace_bytes, stream=0):
+    return _check(lib().spec_verify_tree_sample(
+        target_ptr, draft_ptr, parents_ptr, node_tokens_ptr, uniforms_ptr, B, N, V, D,
+        float(temperature), float(top_p), int(top_k), dtype, out_tokens_ptr, out_num_ptr,
+        out_path_ptr, workspace_ptr, workspace_bytes, stream))
 
 
 def spec_verify_status_string(status):
@@ -429,3 +449,29 @@ def tree_mask(parents, pos0=None, mask=True, bias=False, pos=True, stream=None):
     spec_verify_tree_mask(_ptr(parents), _ptr(pos0), B, N, _ptr(m), _ptr(bs), _ptr(p),
                           _stream(stream))
     return m, bs, p
+
+
+def verify_tree_sample(target, draft, parents, node_tokens, uniforms, depth, temperature=1.0,
+                       top_p=1.0, top_k=0, workspace=None, stream=None):
+    """Tensor-level spec_verify_tree_sample.  Returns (out_tokens [B, D+1],
+    out_num_accepted [B], out_path [B, D+1], workspace)."""
+    torch = _torch()
+    B, N, V = target.shape
+    dt = _dtype_code(target)
+    _need(target, "target", target.dtype, (B, N, V))
+    _need(draft, "draft", target.dtype, (B, N, V))
+    _need(parents, "parents", torch.int32, (N,))
+    _need(node_tokens, "node_tokens", torch.int32, (B, N))
+    _need(uniforms, "uniforms", torch.float32, (B, N))
+    dev = target.device
+    W = depth + 1
+    out_t = torch.empty((B, W), dtype=torch.int32, device=dev)
+    out_n = torch.empty((B,), dtype=torch.int32, device=dev)
+    out_p = torch.empty((B, W), dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = new_workspace(spec_verify_tree_sample_workspace_size(B, N, V), dev)
+    spec_verify_tree_sample(_ptr(target), _ptr(draft), _ptr(parents), _ptr(node_tokens),
+                            _ptr(uniforms), B, N, V, depth, temperature, top_p, top_k, dt,
+                            _ptr(out_t), _ptr(out_n), _ptr(out_p), _ptr(workspace),
+                            workspace.numel(), _stream(stream))
+    return out_t, out_n, out_p, workspace

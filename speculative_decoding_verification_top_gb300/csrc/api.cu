@@ -325,6 +325,86 @@ SPEC_EXPORT int spec_verify_tree(const void *target_logits, const int32_t *paren
     return launch_tree(ta, st);
 }
 
+SPEC_EXPORT int spec_verify_tree_sample_workspace_size(int B, int N, int V, size_t *bytes) {
+    if (!bytes) return SPEC_ERR_NULL;
+    if (!tree_sizes_ok(B, 2 * N, V) || N > SPEC_MAX_TREE_NODES) return SPEC_ERR_SHAPE;
+    *bytes = carve(nullptr, B, 2 * N, V, nullptr, false);
+    return SPEC_OK;
+}
+
+SPEC_EXPORT int spec_verify_tree_sample(const void *target_logits, const void *draft_logits,
+                                        const int32_t *parents, const int32_t *node_tokens,
+                                        const float *uniforms, int B, int N, int V, int D,
+                                        float temperature, float top_p, int top_k, int dtype,
+                                        int32_t *out_tokens, int32_t *out_num_accepted,
+                                        int32_t *out_path, void *workspace,
+                                        size_t workspace_bytes, spec_stream_t stream) {
+    if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_DTYPE;
+    if (N < 1 || N > SPEC_MAX_TREE_NODES || !tree_sizes_ok(B, 2 * N, V) || D < 0 || D >= N)
+        return SPEC_ERR_SHAPE;
+    if (!(temperature > 0.0f) || !std::isfinite(temperature) || !(top_p > 0.0f) ||
+        !(top_p <= 1.0f))
+        return SPEC_ERR_PARAM;
+    if (B == 0) return SPEC_OK;
+    if (!target_logits || !draft_logits || !parents || !node_tokens || !uniforms ||
+        !out_tokens || !out_num_accepted || !workspace)
+        return SPEC_ERR_NULL;
+    const size_t esz = dtype == SPEC_F32 ? 4 : 2;
+    if (!aligned(target_logits, esz) || !aligned(draft_logits, esz) || !aligned(parents, 4) ||
+        !aligned(node_tokens, 4) || !aligned(uniforms, 4) || !aligned(out_tokens, 4) ||
+        !aligned(out_num_accepted, 4) || (out_path && !aligned(out_path, 4)) ||
+        !aligned(workspace, 16))
+        return SPEC_ERR_ALIGN;
+    if (workspace_bytes < carve(nullptr, B, 2 * N, V, nullptr, false)) return SPEC_ERR_WORKSPACE;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    Workspace ws;
+    carve(workspace, B, 2 * N, V, &ws, false);
+    const float c = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
+    // Row statistics of the 2N rows of every sequence (targets, then drafts).
+    RowView rv;
+    rv.target = target_logits;
+    rv.draft = draft_logits;
+    rv.V = V;
+    rv.k = N;
+    rv.R = 2 * N;
+    rv.draft_rows_from = N;
+    rv.tgt_rows_per_seq = N;
+    SeqArgs sq = {};
+    sq.work = kSeqNone;
+    const int kk = top_k > 0 && top_k < V ? top_k : 0;
+    int rc;
+    if (top_p < 1.0f || kk > 0) {
+        ToppArgs ta;
+        ta.rows = rv;
+        ta.seq = sq;
+        ta.c = c;
+        ta.temperature = temperature;
+        ta.top_p = top_p;
+        ta.top_k = kk;
+        ta.ws = ws;
+        rc = launch_topp_rows(ta, B * 2 * N, dtype, st);
+    } else {
+        rc = launch_stream_rows(rv, sq, B * 2 * N, c, ws, 0, dtype, st);
+    }
+    if (rc != SPEC_OK) return rc;
+    TreeSampleArgs a;
+    a.target = target_logits;
+    a.draft = draft_logits;
+    a.parents = parents;
+    a.node_tokens = node_tokens;
+    a.uniforms = uniforms;
+    a.B = B;
+    a.N = N;
+    a.V = V;
+    a.D = D;
+    a.c = c;
+    a.out_tokens = out_tokens;
+    a.out_num = out_num_accepted;
+    a.out_path = out_path;
+    a.ws = ws;
+    return launch_tree_sample(a, dtype, st);
+}
+
 SPEC_EXPORT int spec_verify_tree_mask(const int32_t *parents, const int32_t *pos0, int B, int N,
                                       uint8_t *out_mask, float *out_bias, int32_t *out_pos,
                                       spec_stream_t stream) {

@@ -667,6 +667,20 @@ struct AcceptArgs {
     float *tv;         // [B, k] or null
 };
 
+struct TreeSampleArgs {
+    const void *target;         // [B, N, V]
+    const void *draft;          // [B, N, V]
+    const int32_t *parents;     // [N]
+    const int32_t *node_tokens; // [B, N]
+    const float *uniforms;      // [B, N]: 0 the final draw, c node c's test
+    int B, N, V, D;
+    float c;                    // log2(e) / temperature
+    int32_t *out_tokens;
+    int32_t *out_num;
+    int32_t *out_path;
+    Workspace ws;               // row records [B, 2N]: target rows, then draft rows
+};
+
 struct TreeMaskArgs {
     const int32_t *parents;  // [B, N]
     const int32_t *pos0;     // [B] or null (0)
@@ -719,6 +733,8 @@ int launch_topp_rows(const ToppArgs &a, int rows_total, int dtype, cudaStream_t 
 // The final kernel is launched as a programmatic dependent of the row kernel.
 int launch_final(const FinalArgs &a, int dtype, cudaStream_t st);
 int launch_tree(const TreeArgs &a, cudaStream_t st);
+// Stochastic tree walk over the row records (treesample.cu).
+int launch_tree_sample(const TreeSampleArgs &a, int dtype, cudaStream_t st);
 // Tree attention mask / bias / positions for B trees (treemask.cu).
 int launch_tree_mask(const TreeMaskArgs &a, cudaStream_t st);
 // Acceptance rate per (sequence, position) from a verify call's row records;

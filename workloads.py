@@ -265,4 +265,41 @@ def c5(seed=5, B=16, V=32000, branching=4, depth=3, dtype=F32):
     return Tree("c5", B, N, V, depth, dtype, target, parents, node_tokens)
 
 
+@dataclass
+class SampledTree:
+    """One stochastic tree-verification batch (spec_verify_tree_sample)."""
+    name: str
+    B: int
+    N: int
+    V: int
+    D: int
+    dtype: str
+    T: float
+    target: np.ndarray        # [B, N, V]
+    draft: np.ndarray         # [B, N, V]: row n drew node n's children
+    parents: np.ndarray       # [N] int32
+    node_tokens: np.ndarray   # [B, N] int32
+    uniforms: np.ndarray      # [B, N] float32: 0 the final draw, c node c's test
+
+    def logit_bytes(self):
+        return 2 * self.B * self.N * self.V * (4 if self.dtype == F32 else 2)
+
+
+def c5s(seed=55, B=16, V=32000, branching=4, depth=3, dtype=F32, T=1.0, noise=1.0):
+    """c5's tree shape and target generator, sampled: draft = target + N(0,
+    noise^2); every node's children drawn independently (Gumbel-max over
+    draft row / T) from its draft row; uniforms for every node."""
+    r_logit, r_draft, r_u = _streams(seed)
+    parents = bfs_parents(branching, depth)
+    N = parents.shape[0]
+    tgt = zipf_gauss(r_logit, B * N, V, 1.5).reshape(B, N, V)
+    drf = (tgt + r_draft.normal(0.0, noise, tgt.shape)).astype(np.float32)
+    node_tokens = np.zeros((B, N), np.int32)
+    par = parents.astype(np.int64)
+    for n in range(1, N):
+        node_tokens[:, n] = gumbel_draw(r_draft, drf[:, par[n]], T)
+    return SampledTree("c5s", B, N, V, depth, dtype, T, _store(tgt, dtype), _store(drf, dtype),
+                       parents, node_tokens, uniforms(r_u, (B, N)))
+
+
 CONFIGS = {"c1": c1, "c2": c2, "c3": c3, "c4": c4, "c5": c5}
