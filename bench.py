@@ -429,6 +429,40 @@ def timed_topk(job, K=50, launches=200):
             "achieved_gbs": round(nbytes / (ms * 1e-3) / 1e9, 1)}
 
 
+def timed_tree_sample(job, launches=100):
+    """spec_verify_tree_sample on c5's tree shape, sampled (draft rows =
+    target + noise, children drawn from their parent's draft row): device
+    time per call."""
+    import torch
+    sv = job.sv
+    tr = workloads.c5s(B=job.wl.B, V=job.wl.V)
+    dt = sv.SPEC_BF16 if tr.dtype == workloads.BF16 else sv.SPEC_F32
+    tg, dr = to_dev(tr.target, job.dev), to_dev(tr.draft, job.dev)
+    par, tok = to_dev(tr.parents, job.dev), to_dev(tr.node_tokens, job.dev)
+    uni = to_dev(tr.uniforms, job.dev)
+    W = tr.D + 1
+    ot = torch.empty((tr.B, W), dtype=torch.int32, device=job.dev)
+    on = torch.empty((tr.B,), dtype=torch.int32, device=job.dev)
+    op = torch.empty((tr.B, W), dtype=torch.int32, device=job.dev)
+    ws = sv.new_workspace(sv.spec_verify_tree_sample_workspace_size(tr.B, tr.N, tr.V), job.dev)
+
+    def one(i):
+        sv.spec_verify_tree_sample(tg.data_ptr(), dr.data_ptr(), par.data_ptr(), tok.data_ptr(),
+                                   uni.data_ptr(), tr.B, tr.N, tr.V, tr.D, tr.T, 1.0, 0, dt,
+                                   ot.data_ptr(), on.data_ptr(), op.data_ptr(), ws.data_ptr(),
+                                   ws.numel(), job.stream.cuda_stream)
+
+    for i in range(3):
+        one(i)
+    torch.cuda.synchronize()
+    ms = device_launch_ms(one, launches, job.stream)
+    depths = np.bincount(np.maximum(on.cpu().numpy(), 0), minlength=W).tolist()
+    nbytes = tr.logit_bytes()
+    return {"entry": "spec_verify_tree_sample", "B": tr.B, "N": tr.N, "V": tr.V,
+            "avg_call_us": round(ms * 1e3, 2), "bytes_rows": nbytes,
+            "achieved_gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "depth_hist": depths}
+
+
 def timed_e2e(job, steps):
     """Host buffers -> device -> library call -> results back to the host."""
     import torch
@@ -521,6 +555,7 @@ def run_ours(args):
     probs = timed_probs(job) if mode != "tree" else None
     topk = timed_topk(job) if mode != "tree" else None
     tmask = timed_tree_mask(job) if mode == "tree" else None
+    tsample = timed_tree_sample(job) if mode == "tree" else None
     total_ms = max_over_ranks(total_ms, world)
 
     nbytes = wl.logit_bytes(mode)
@@ -576,6 +611,8 @@ def run_ours(args):
         out["acceptance"] = accept
     if tmask is not None:
         out["tree_mask"] = tmask
+    if tsample is not None:
+        out["tree_sample"] = tsample
     if topk is not None:
         topk["frac"] = round(topk["achieved_gbs"] / peak, 4)
         out["top_k"] = topk
