@@ -14,18 +14,26 @@
 //
 // Row statistics (max, normaliser, nucleus key) of the 2N rows of every
 // sequence come from the row kernels.  tree_sample_kernel then walks each
-// sequence with one CTA: a rejected child costs one pass over the node's two
-// rows (the residual's normaliser), the final draw two (total, then the
-// crossing).  p'(x) is never stored: it is rebuilt from p(x), q(x) and the
-// normalisers so far, p'_{j+1}(x) = max(0, p'_j(x) - q(x)) / S_{j+1}.  Sums
-// run over 256 contiguous per-thread chunks in a fixed order.
+// sequence with one cluster of 8 CTAs (8 SMs), each streaming one slice of
+// the vocabulary: a rejected child costs one pass over the node's two rows
+// (the residual's normaliser), the final draw one more (the total) plus a
+// rescan of one chunk.  p'(x) is never stored: it is rebuilt from p(x), q(x)
+// and the normalisers so far, p'_{j+1}(x) = max(0, p'_j(x) - q(x)) /
+// S_{j+1}.  Sums run over contiguous per-thread chunks in a fixed order,
+// CTA totals are added in rank order through distributed shared memory,
+// and the cluster barrier is the only wait.
+
+#include <cooperative_groups.h>
 
 #include "common.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace specv {
 namespace {
 
 constexpr int kTsThreads = 256;
+constexpr int kTsCluster = 8;  // CTAs per sequence (one cluster), each a slice of V
 constexpr int kTsMaxRej = 64;  // residual rounds kept per node (children tried)
 
 struct TsShared {
@@ -34,6 +42,7 @@ struct TsShared {
     int nkids[SPEC_MAX_TREE_NODES];
     float inv_s[kTsMaxRej];   // 1 / S_j of the residual rounds at the current node
     float part[kTsThreads];   // per-thread chunk sums
+    float ctot[2];            // this CTA's total of the current pass (two slots, alternating)
     float total, pre;
     int bad_flags;
     int cross, token;
@@ -108,20 +117,39 @@ __device__ float block_sum_ordered(TsShared &sh, float v) {
     return sh.total;
 }
 
+// The cluster's sum of one value per thread: each CTA adds its threads' in
+// thread order, then every CTA adds the CTAs' totals in rank order (read
+// from their shared memory), so every thread of the cluster gets the same
+// total.  `slot` alternates between passes: a CTA writes a slot again only
+// two passes later, after a cluster barrier every reader has passed.
+__device__ float cluster_sum(TsShared &sh, cg::cluster_group &cl, float v, int slot) {
+    const float mine = block_sum_ordered(sh, v);
+    if (threadIdx.x == 0) sh.ctot[slot] = mine;
+    cl.sync();
+    float s = 0.0f;
+    for (int r = 0; r < kTsCluster; ++r) s = __fadd_rn(s, *cl.map_shared_rank(&sh.ctot[slot], r));
+    return s;
+}
+
+// One cluster of kTsCluster CTAs per sequence; CTA r owns the r-th slice of
+// the vocabulary, split into contiguous per-thread chunks.  Every CTA takes
+// the same decisions (the same inputs and totals); rank 0 writes the path,
+// the CTA whose slice holds the final draw's crossing writes that token.
 template <typename T>
 __global__ void __launch_bounds__(kTsThreads) tree_sample_kernel(const TreeSampleArgs a) {
     __shared__ TsShared sh;
-    const int b = blockIdx.x, tid = threadIdx.x, N = a.N, V = a.V, W = a.D + 1;
+    cg::cluster_group cl = cg::this_cluster();
+    const int rank = static_cast<int>(cl.block_rank());
+    const int b = blockIdx.x / kTsCluster, tid = threadIdx.x, N = a.N, V = a.V, W = a.D + 1;
     const float c = a.c;
     const RowRec *rr = a.ws.rows + static_cast<size_t>(b) * 2 * N;
     const T *tgt = static_cast<const T *>(a.target) + static_cast<size_t>(b) * N * V;
     const T *drf = static_cast<const T *>(a.draft) + static_cast<size_t>(b) * N * V;
     const float *ub = a.uniforms + static_cast<size_t>(b) * N;
     if (tid == 0) sh.bad_flags = 0;
-    __syncthreads();
-    uint32_t bad = 0;
     for (int n = tid; n < N; n += kTsThreads) sh.nkids[n] = 0;
     __syncthreads();
+    uint32_t bad = 0;
     for (int n = tid; n < N; n += kTsThreads) {
         const int p = a.parents[n];
         sh.par[n] = p;
@@ -150,23 +178,28 @@ __global__ void __launch_bounds__(kTsThreads) tree_sample_kernel(const TreeSampl
     int32_t *ot = a.out_tokens + static_cast<size_t>(b) * W;
     int32_t *op = a.out_path ? a.out_path + static_cast<size_t>(b) * W : nullptr;
     if (sh.bad_flags) {
-        for (int i = tid; i < W; i += kTsThreads) {
-            ot[i] = -1;
-            if (op) op[i] = -1;
-        }
-        if (tid == 0) {
-            a.out_num[b] = -1;
-            atomicOr(a.ws.err, static_cast<uint32_t>(sh.bad_flags));
+        // Every CTA of the cluster found the same flags: all leave here.
+        if (rank == 0) {
+            for (int i = tid; i < W; i += kTsThreads) {
+                ot[i] = -1;
+                if (op) op[i] = -1;
+            }
+            if (tid == 0) {
+                a.out_num[b] = -1;
+                atomicOr(a.ws.err, static_cast<uint32_t>(sh.bad_flags));
+            }
         }
         return;
     }
-    // This thread's contiguous chunk of the vocabulary (a multiple of four
+    // This CTA's slice and this thread's chunk of it (multiples of four
     // vectors, so that every chunk starts 16-byte aligned when rows do).
     constexpr int VE = Elem<T>::kPerVec;
-    const int per = ((V + kTsThreads - 1) / kTsThreads + 4 * VE - 1) / (4 * VE) * (4 * VE);
-    const int x0 = min(V, tid * per), x1 = min(V, x0 + per);
-    int cur = 0, depth = 0;
-    if (tid == 0 && op) op[0] = 0;
+    const int span = ((V + kTsCluster - 1) / kTsCluster + 4 * VE - 1) / (4 * VE) * (4 * VE);
+    const int s0 = min(V, rank * span), s1 = min(V, s0 + span);
+    const int per = ((span + kTsThreads - 1) / kTsThreads + 4 * VE - 1) / (4 * VE) * (4 * VE);
+    const int x0 = min(s1, s0 + tid * per), x1 = min(s1, x0 + per);
+    int cur = 0, depth = 0, pass = 0;
+    if (rank == 0 && tid == 0 && op) op[0] = 0;
     for (;;) {
         const RowP P = row_p(rr + cur, c), Q = row_p(rr + N + cur, c);
         const T *prow = tgt + static_cast<size_t>(cur) * V;
@@ -191,7 +224,7 @@ __global__ void __launch_bounds__(kTsThreads) tree_sample_kernel(const TreeSampl
                 const float q = proc_prob<T>(l2, c, Q.neg, Q.inv, Q.lam);
                 s = __fadd_rn(s, fmaxf(__fsub_rn(v, q), 0.0f));
             });
-            const float S = block_sum_ordered(sh, s);
+            const float S = cluster_sum(sh, cl, s, pass++ & 1);
             if (S > 0.0f && nrej < kTsMaxRej) {
                 if (tid == 0) sh.inv_s[nrej] = __frcp_rn(S);
                 __syncthreads();
@@ -199,7 +232,7 @@ __global__ void __launch_bounds__(kTsThreads) tree_sample_kernel(const TreeSampl
             }
         }
         if (next >= 0) {
-            if (tid == 0) {
+            if (rank == 0 && tid == 0) {
                 ot[depth] = sh.tok[next];
                 if (op) op[depth + 1] = next;
             }
@@ -207,36 +240,70 @@ __global__ void __launch_bounds__(kTsThreads) tree_sample_kernel(const TreeSampl
             cur = next;
             continue;
         }
-        // Final draw from p': the total over fixed chunks, then the chunk
-        // holding u * S rescanned in the same order.
+        // Final draw from p': the total over fixed chunks, then the slice
+        // and the chunk holding u * S, the chunk rescanned in the same order.
         float s = 0.0f;
         chunk_for<T>(prow, qrow, x0, x1, vec, [&](float l1, float l2, int) {
             s = __fadd_rn(s, resid_prob<T>(l1, l2, c, P, Q, sh.inv_s, nrej));
         });
-        const float S = block_sum_ordered(sh, s);
+        const int slot = pass & 1;
+        const float S = cluster_sum(sh, cl, s, slot);
         const float target = __fmul_rn(ub[0], S);
-        if (tid == 0) sh.token = -1;
-        __syncthreads();
+        // The slice whose running prefix (in rank order, as S was summed)
+        // first passes the target; else the last slice with weight.
+        float ptot[kTsCluster];
+        for (int r = 0; r < kTsCluster; ++r) ptot[r] = *cl.map_shared_rank(&sh.ctot[slot], r);
+        // No CTA leaves while another may still read its shared memory.
+        cl.sync();
+        float pre = 0.0f, pre_last = 0.0f;
+        int rc = -1, rlast = -1;
+        for (int r = 0; r < kTsCluster; ++r) {
+            const float nx = __fadd_rn(pre, ptot[r]);
+            if (ptot[r] > 0.0f) {
+                rlast = r;
+                pre_last = pre;
+                if (rc < 0 && nx > target) {
+                    rc = r;
+                    break;
+                }
+            }
+            pre = nx;
+        }
+        if (rc < 0) {
+            rc = rlast;
+            pre = pre_last;
+        }
+        if (rank == 0 && tid == 0) {
+            for (int i = depth + 1; i < W; ++i) {
+                ot[i] = -1;
+                if (op) op[i] = -1;
+            }
+            a.out_num[b] = depth;
+            if (rc < 0) ot[depth] = -1;
+        }
+        if (rank != rc) return;
         if (tid == 0) {
-            // The first chunk whose running prefix passes the target (the
-            // prefix summed in thread order, as the total was).
-            float pre = 0.0f;
+            // The first chunk of this slice whose running prefix passes the
+            // target, else the last chunk with weight.
+            float run = pre;
             int t = 0, lastnz = -1;
+            float run_last = pre;
             for (; t < kTsThreads; ++t) {
-                const float nx = __fadd_rn(pre, sh.part[t]);
-                if (sh.part[t] > 0.0f) lastnz = t;
-                if (nx > target && sh.part[t] > 0.0f) break;
-                pre = nx;
+                const float nx = __fadd_rn(run, sh.part[t]);
+                if (sh.part[t] > 0.0f) {
+                    lastnz = t;
+                    run_last = run;
+                    if (nx > target) break;
+                }
+                run = nx;
             }
             if (t == kTsThreads) {
-                // Rounding left u * S at the very end: the last chunk with
-                // weight, entered at its own prefix.
                 t = lastnz;
-                pre = 0.0f;
-                for (int i = 0; i < t; ++i) pre = __fadd_rn(pre, sh.part[i]);
+                run = run_last;
             }
-            sh.pre = pre;
+            sh.pre = run;
             sh.cross = t;
+            sh.token = -1;
         }
         __syncthreads();
         const int tc = sh.cross;
@@ -254,14 +321,7 @@ __global__ void __launch_bounds__(kTsThreads) tree_sample_kernel(const TreeSampl
             sh.token = tok >= 0 ? tok : last;
         }
         __syncthreads();
-        if (tid == 0) {
-            ot[depth] = sh.token;
-            for (int i = depth + 1; i < W; ++i) {
-                ot[i] = -1;
-                if (op) op[i] = -1;
-            }
-            a.out_num[b] = depth;
-        }
+        if (tid == 0) ot[depth] = sh.token;
         return;
     }
 }
@@ -269,11 +329,20 @@ __global__ void __launch_bounds__(kTsThreads) tree_sample_kernel(const TreeSampl
 }  // namespace
 
 int launch_tree_sample(const TreeSampleArgs &a, int dtype, cudaStream_t st) {
-    if (dtype == SPEC_F32)
-        tree_sample_kernel<float><<<a.B, kTsThreads, 0, st>>>(a);
-    else
-        tree_sample_kernel<uint16_t><<<a.B, kTsThreads, 0, st>>>(a);
-    return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(a.B) * kTsCluster);
+    cfg.blockDim = dim3(kTsThreads);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kTsCluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = dtype == SPEC_F32 ? cudaLaunchKernelEx(&cfg, tree_sample_kernel<float>, a)
+                                            : cudaLaunchKernelEx(&cfg, tree_sample_kernel<uint16_t>, a);
+    return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
 }  // namespace specv
