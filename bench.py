@@ -215,7 +215,7 @@ class Job:
         self.sets = []
         if mode == "tree":
             base = (to_dev(wl.target, dev), to_dev(wl.parents, dev), to_dev(wl.node_tokens, dev))
-            self.sets = [base, (base[0].clone(), base[1], base[2])]
+            self.sets = [base, tuple(a.clone() for a in base)]
             W = wl.D + 1
             self.out_t = torch.empty((wl.B, W), dtype=torch.int32, device=dev)
             self.out_n = torch.empty((wl.B,), dtype=torch.int32, device=dev)
@@ -225,7 +225,7 @@ class Job:
         else:
             base = (to_dev(wl.target, dev), to_dev(wl.draft, dev), to_dev(wl.draft_tokens, dev),
                     to_dev(wl.uniforms, dev))
-            self.sets = [base, (base[0].clone(), base[1].clone(), base[2], base[3])]
+            self.sets = [base, tuple(a.clone() for a in base)]
             self.out_t = torch.empty((wl.B, wl.k + 1), dtype=torch.int32, device=dev)
             self.out_n = torch.empty((wl.B,), dtype=torch.int32, device=dev)
             nbytes = sv.spec_verify_workspace_size(wl.B, wl.k, wl.V)
@@ -464,7 +464,10 @@ def timed_tree_sample(job, launches=100):
 
 
 def timed_e2e(job, steps):
-    """Host buffers -> device -> library call -> results back to the host."""
+    """Host buffers -> device -> library call -> results back to the host,
+    every step.  Two device input sets alternate: the copy of step i+1 (its
+    own stream) overlaps the call and the read-back of step i; a copy into a
+    set waits until the call that last read it has finished."""
     import torch
     wl = job.wl
     def pinned(a):
@@ -479,28 +482,40 @@ def timed_e2e(job, steps):
     else:
         host_in = [pinned(a) for a in (wl.target, wl.draft, wl.draft_tokens, wl.uniforms)]
         outs = (job.out_t, job.out_n)
-    dev_in = job.sets[0]
     host_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
-    views = [d.view(torch.int16) if d.dtype == torch.bfloat16 else d for d in dev_in]
+    views = [[d.view(torch.int16) if d.dtype == torch.bfloat16 else d for d in job.sets[j]]
+             for j in range(2)]
     h2d = sum(h.numel() * h.element_size() for h in host_in)
     d2h = sum(h.numel() * h.element_size() for h in host_out)
+    copy_stream = torch.cuda.Stream(device=job.dev)
+    copied = [torch.cuda.Event(), torch.cuda.Event()]
+    done = [torch.cuda.Event(), torch.cuda.Event()]
+    for e in done:
+        e.record(job.stream)
 
-    def one():
-        for h, d in zip(host_in, views):
-            d.copy_(h, non_blocking=True)
-        job.step(0)
+    def one(i):
+        j = i % 2
+        copy_stream.wait_event(done[j])
+        with torch.cuda.stream(copy_stream):
+            for h, d in zip(host_in, views[j]):
+                d.copy_(h, non_blocking=True)
+        copied[j].record(copy_stream)
+        job.stream.wait_event(copied[j])
+        job.step(j)
         for h, o in zip(host_out, outs):
             h.copy_(o, non_blocking=True)
+        done[j].record(job.stream)
 
-    for _ in range(3):
-        one()
+    for i in range(4):
+        one(i)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     t0 = time.perf_counter()
     e0.record(job.stream)
-    for _ in range(steps):
-        one()
+    copy_stream.wait_event(e0)
+    for i in range(steps):
+        one(i)
     e1.record(job.stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
