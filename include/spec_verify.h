@@ -31,7 +31,8 @@
  *     matching *_workspace_size function reports.  It must be zero-filled
  *     before its first use (spec_verify_workspace_init, or any zero fill);
  *     the library returns its internal counters to zero at the end of every
- *     call.  Calls that share one workspace must be ordered (one stream, or
+ *     call.  After a call that returned SPEC_ERR_CUDA, zero-fill it again.
+ *     Calls that share one workspace must be ordered (one stream, or
  *     events): two calls running at the same time on one workspace race.
  */
 #ifndef SPEC_VERIFY_H

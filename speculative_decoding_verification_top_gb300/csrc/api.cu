@@ -19,7 +19,8 @@ int pmax_for(int V) { return (V + kMinSeg - 1) / kMinSeg + 2; }
 // Carve the workspace; returns the bytes needed (base may be null).
 // `chain`: a chain call (rows_per_seq = 2k+1), which also needs the top-p
 // nucleus lists of its B (k+1) target rows; a tree call does not.
-size_t carve(void *base, int B, int rows_per_seq, int V, Workspace *ws, bool chain) {
+size_t carve(void *base, int B, int rows_per_seq, int V, Workspace *ws, bool chain,
+             bool capture) {
     const size_t rows = static_cast<size_t>(B) * rows_per_seq;
     const int pmax = pmax_for(V), NS = subs_for(V);
     size_t off = 0;
@@ -41,6 +42,7 @@ size_t carve(void *base, int B, int rows_per_seq, int V, Workspace *ws, bool cha
     char *nuc = take(trows * kNucCap * sizeof(uint4));
     const size_t pairs = chain ? static_cast<size_t>(B) * ((rows_per_seq - 1) / 2) : 0;
     char *accq = take(chain ? (pairs + 2) * sizeof(uint32_t) : 0);
+    char *sum = take(capture ? rows * sum_stride_for(V) * sizeof(uint32_t) : 0);
     if (ws) {
         ws->err = reinterpret_cast<uint32_t *>(err);
         ws->row_ctr = reinterpret_cast<uint32_t *>(row_ctr);
@@ -53,6 +55,8 @@ size_t carve(void *base, int B, int rows_per_seq, int V, Workspace *ws, bool cha
         ws->nuc_n = reinterpret_cast<int32_t *>(nuc_n);
         ws->nuc = reinterpret_cast<uint4 *>(nuc);
         ws->accq = reinterpret_cast<uint32_t *>(accq);
+        ws->sum = reinterpret_cast<uint32_t *>(sum);
+        ws->sum_stride = sum_stride_for(V);
         ws->pmax = pmax;
     }
     return off;
@@ -104,7 +108,8 @@ int plan_chain(const void *target_logits, const void *draft_logits, const int32_
         !aligned(draft_tokens, 4) || (stoch && !aligned(uniforms, 4)) ||
         !aligned(out_tokens, 4) || !aligned(out_num_accepted, 4) || !aligned(workspace, 16))
         return SPEC_ERR_ALIGN;
-    if (workspace_bytes < carve(nullptr, B, 2 * k + 1, V, nullptr, true)) return SPEC_ERR_WORKSPACE;
+    if (workspace_bytes < carve(nullptr, B, 2 * k + 1, V, nullptr, true, true))
+        return SPEC_ERR_WORKSPACE;
 
     plan->stoch = stoch;
     plan->dtype = dtype;
@@ -115,7 +120,7 @@ int plan_chain(const void *target_logits, const void *draft_logits, const int32_
     plan->use_topp = stoch && (top_p < 1.0f || plan->top_k > 0);
     plan->c = static_cast<float>(1.4426950408889634 / static_cast<double>(plan->temperature));
     plan->st = reinterpret_cast<cudaStream_t>(stream);
-    carve(workspace, B, 2 * k + 1, V, &plan->ws, true);
+    carve(workspace, B, 2 * k + 1, V, &plan->ws, true, true);
 
     RowView &rv = plan->rows;
     rv.target = target_logits;
@@ -183,14 +188,14 @@ using namespace specv;
 SPEC_EXPORT int spec_verify_workspace_size(int B, int k, int V, size_t *bytes) {
     if (!bytes) return SPEC_ERR_NULL;
     if (!chain_sizes_ok(B, k, V)) return SPEC_ERR_SHAPE;
-    *bytes = carve(nullptr, B, 2 * k + 1, V, nullptr, true);
+    *bytes = carve(nullptr, B, 2 * k + 1, V, nullptr, true, true);
     return SPEC_OK;
 }
 
 SPEC_EXPORT int spec_verify_tree_workspace_size(int B, int N, int V, size_t *bytes) {
     if (!bytes) return SPEC_ERR_NULL;
     if (!tree_sizes_ok(B, N, V)) return SPEC_ERR_SHAPE;
-    *bytes = carve(nullptr, B, N, V, nullptr, false);
+    *bytes = carve(nullptr, B, N, V, nullptr, false, false);
     return SPEC_OK;
 }
 
@@ -294,11 +299,11 @@ SPEC_EXPORT int spec_verify_tree(const void *target_logits, const int32_t *paren
         !aligned(out_tokens, 4) || !aligned(out_num_accepted, 4) ||
         (out_path && !aligned(out_path, 4)) || !aligned(workspace, 16))
         return SPEC_ERR_ALIGN;
-    if (workspace_bytes < carve(nullptr, B, N, V, nullptr, false)) return SPEC_ERR_WORKSPACE;
+    if (workspace_bytes < carve(nullptr, B, N, V, nullptr, false, false)) return SPEC_ERR_WORKSPACE;
 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     Workspace ws;
-    carve(workspace, B, N, V, &ws, false);
+    carve(workspace, B, N, V, &ws, false, false);
     RowView rv;
     rv.target = target_logits;
     rv.draft = nullptr;
@@ -328,7 +333,7 @@ SPEC_EXPORT int spec_verify_tree(const void *target_logits, const int32_t *paren
 SPEC_EXPORT int spec_verify_tree_sample_workspace_size(int B, int N, int V, size_t *bytes) {
     if (!bytes) return SPEC_ERR_NULL;
     if (!tree_sizes_ok(B, 2 * N, V) || N > SPEC_MAX_TREE_NODES) return SPEC_ERR_SHAPE;
-    *bytes = carve(nullptr, B, 2 * N, V, nullptr, false);
+    *bytes = carve(nullptr, B, 2 * N, V, nullptr, false, true);
     return SPEC_OK;
 }
 
@@ -355,10 +360,10 @@ SPEC_EXPORT int spec_verify_tree_sample(const void *target_logits, const void *d
         !aligned(out_num_accepted, 4) || (out_path && !aligned(out_path, 4)) ||
         !aligned(workspace, 16))
         return SPEC_ERR_ALIGN;
-    if (workspace_bytes < carve(nullptr, B, 2 * N, V, nullptr, false)) return SPEC_ERR_WORKSPACE;
+    if (workspace_bytes < carve(nullptr, B, 2 * N, V, nullptr, false, true)) return SPEC_ERR_WORKSPACE;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     Workspace ws;
-    carve(workspace, B, 2 * N, V, &ws, false);
+    carve(workspace, B, 2 * N, V, &ws, false, true);
     const float c = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
     // Row statistics of the 2N rows of every sequence (targets, then drafts).
     RowView rv;
@@ -446,10 +451,11 @@ SPEC_EXPORT int spec_verify_intermediates(const void *workspace, size_t workspac
                                           spec_stream_t stream) {
     if (!workspace) return SPEC_ERR_NULL;
     if (!chain_sizes_ok(B, k, V)) return SPEC_ERR_SHAPE;
-    if (workspace_bytes < carve(nullptr, B, 2 * k + 1, V, nullptr, true)) return SPEC_ERR_WORKSPACE;
+    if (workspace_bytes < carve(nullptr, B, 2 * k + 1, V, nullptr, true, true))
+        return SPEC_ERR_WORKSPACE;
     if (B == 0) return SPEC_OK;
     Workspace ws;
-    carve(const_cast<void *>(workspace), B, 2 * k + 1, V, &ws, true);
+    carve(const_cast<void *>(workspace), B, 2 * k + 1, V, &ws, true, true);
     return launch_intermediates(ws, B, k, P, Q, Z, S, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -469,9 +475,10 @@ SPEC_EXPORT int spec_verify_acceptance(const void *target_logits, const void *dr
     if (!aligned(target_logits, esz) || !aligned(draft_logits, esz) || !aligned(out_beta, 4) ||
         (out_tv && !aligned(out_tv, 4)) || !aligned(workspace, 16))
         return SPEC_ERR_ALIGN;
-    if (workspace_bytes < carve(nullptr, B, 2 * k + 1, V, nullptr, true)) return SPEC_ERR_WORKSPACE;
+    if (workspace_bytes < carve(nullptr, B, 2 * k + 1, V, nullptr, true, true))
+        return SPEC_ERR_WORKSPACE;
     AcceptArgs a;
-    carve(workspace, B, 2 * k + 1, V, &a.ws, true);
+    carve(workspace, B, 2 * k + 1, V, &a.ws, true, true);
     a.rows.target = target_logits;
     a.rows.draft = draft_logits;
     a.rows.V = V;

@@ -77,6 +77,8 @@ struct Workspace {
     int32_t *nuc_n;        // [B (k+1)] entries of each target row's nucleus list, or -1 (top-p)
     uint4 *nuc;            // [B (k+1), kNucCap] (index, target logit, draft logit at it), index order
     uint32_t *accq;        // acceptance queue: [0] length, [1] CTA arrivals, then [B k] pair ids
+    uint32_t *sum;         // [rows, sum_stride] row summaries, one entry per group (top-p / top-k)
+    int sum_stride;        // summary entries per row
     int pmax;              // partial slots per row
 };
 
@@ -247,6 +249,11 @@ __device__ __forceinline__ uint32_t okey(float v) {
     return sizeof(T) == 2 ? (b >> 16) : b;
 }
 
+// The float whose okey<float> is k.
+__device__ __forceinline__ float key_float(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
 // Processed probability of one logit: [key >= lam] 2^(l c - m c) / z, with
 // negmc = -(m c) and invz = 1 / z.  Explicit round-to-nearest intrinsics
 // keep every call site bitwise identical.
@@ -322,6 +329,90 @@ struct Span {
         a1 = a0 + nvec * P;
     }
 };
+
+// ------------------------------------------------------ row summaries
+//
+// A statistics pass over a row also leaves its summary: for every group of
+// logits one lane reduced in one batch (kBatch vectors, 32 lanes apart),
+// one 32-bit entry: bits 31..16 the group's max, bits 15..2 a bound on the
+// max of its other vectors, bits 1..0 the vector holding the max.  Values
+// are rounded up to bf16 and stored as 16-bit ordered keys (the bound
+// keeps the top 14 bits, rounded up).  A later pass then finds the logits
+// above any threshold by reading the summary (one entry per 32 or 16
+// logits) and only the vectors that can reach it: mostly one per group.
+// A row is split into pieces by the warp segments [w seg, (w+1) seg) of the
+// concatenated rows; piece i's groups are stored after those of pieces
+// 0..i-1, batch-major (entry b 32 + lane).
+
+constexpr int kGroupVecs = 32 * kBatch;  // vectors per batch of one warp
+
+// Summary entries reserved per row: enough for any segment length >=
+// kMinSeg and 4- or 2-byte logits.
+__host__ __device__ inline int sum_stride_for(int V) {
+    return ((V + 4 * kGroupVecs - 1) / (4 * kGroupVecs) + V / kMinSeg + 3) * 32;
+}
+
+// Piece i of row `row` (rows of V logits, segments of seg): [lo, hi).
+__device__ __forceinline__ void piece_bounds(int row, int V, long long seg, long long w, int &lo,
+                                             int &hi) {
+    const long long rbase = static_cast<long long>(row) * V;
+    const long long a = w * seg > rbase ? w * seg : rbase;
+    const long long b = (w + 1) * seg < rbase + V ? (w + 1) * seg : rbase + V;
+    lo = static_cast<int>(a - rbase);
+    hi = static_cast<int>(b - rbase);
+}
+
+// Summary entries of one piece.
+template <typename T>
+__device__ __forceinline__ int piece_groups(const T *rowp, int lo, int hi) {
+    const Span<T> sp(rowp, lo, hi);
+    return (sp.nvec + kGroupVecs - 1) / kGroupVecs * 32;
+}
+
+// Summary offset of the piece of `row` in segment w (the sum over the
+// row's earlier pieces).
+template <typename T>
+__device__ __forceinline__ int piece_sum_offset(const T *rowp, int row, int V, long long seg,
+                                                long long w) {
+    const long long wf = static_cast<long long>(row) * V / seg;
+    int off = 0;
+    for (long long w2 = wf; w2 < w; ++w2) {
+        int lo, hi;
+        piece_bounds(row, V, seg, w2, lo, hi);
+        off += piece_groups<T>(rowp, lo, hi);
+    }
+    return off;
+}
+
+// Summary key of a value: the 16-bit ordered key of the smallest bf16
+// value >= x (x itself for bf16 logits).
+__device__ __forceinline__ uint16_t sum_key(float x) {
+    uint32_t b = __float_as_uint(x);
+    if (!(b & 0x80000000u)) b += 0xFFFFu;  // positive: away from zero (no carry out of bit 31)
+    b &= 0xFFFF0000u;                      // negative: toward zero; both round up
+    return static_cast<uint16_t>(okey<float>(__uint_as_float(b)) >> 16);
+}
+
+// The bf16 value (as float) whose summary key is k.
+__device__ __forceinline__ float sum_value(uint32_t k) { return key_float(k << 16); }
+
+// A summary entry from the kBatch vector maxima of one group.
+__device__ __forceinline__ uint32_t sum_entry(const float (&mu)[kBatch]) {
+    static_assert(kBatch == 4, "two bits name the vector");
+    int u1 = 0;
+#pragma unroll
+    for (int u = 1; u < kBatch; ++u)
+        if (!(mu[u] <= mu[u1])) u1 = u;  // the first max (a NaN wins)
+    float rest = kNegInf;
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u)
+        if (u != u1) rest = max_nan(rest, mu[u]);
+    const uint32_t k2 = min((static_cast<uint32_t>(sum_key(rest)) + 3u) >> 2, 0x3FFFu);
+    return (static_cast<uint32_t>(sum_key(mu[u1])) << 16) | (k2 << 2) | static_cast<uint32_t>(u1);
+}
+__device__ __forceinline__ float entry_max(uint32_t e) { return sum_value(e >> 16); }
+__device__ __forceinline__ float entry_rest(uint32_t e) { return sum_value(e & 0xFFFCu); }
+__device__ __forceinline__ int entry_vec(uint32_t e) { return static_cast<int>(e & 3u); }
 
 // Warp scan of one value per lane: exclusive prefix in lane order, and the
 // round total defined as (exclusive prefix of lane 31) + (its value).
@@ -637,6 +728,7 @@ struct ToppArgs {
     SeqArgs seq;
     float c, temperature, top_p;
     int top_k;         // keep the top_k largest logits and their ties first (0: off)
+    long long seg;     // warp segment of the statistics grid (the summaries' layout)
     Workspace ws;
 };
 
@@ -704,8 +796,8 @@ struct TreeArgs {
 // Resident CTAs of `kernel` (kThreads threads) on the current device,
 // cached per device and `slot`; 0 on a CUDA error.
 template <typename K>
-int resident_ctas(K kernel, int slot) {
-    constexpr int kMaxDev = 64, kSlots = 8;
+int resident_ctas(K kernel, int slot, size_t dsmem = 0) {
+    constexpr int kMaxDev = 64, kSlots = 12;
     static int cache[kMaxDev][kSlots];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev || slot < 0 ||
@@ -715,7 +807,7 @@ int resident_ctas(K kernel, int slot) {
     if (v > 0) return v;
     int sms = 0, per_sm = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0) !=
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, dsmem) !=
             cudaSuccess)
         return 0;
     v = sms * (per_sm > 0 ? per_sm : 1);
@@ -727,6 +819,10 @@ int resident_ctas(K kernel, int slot) {
 // SPEC_BF16.  Each returns SPEC_OK or SPEC_ERR_CUDA.
 int launch_stream_rows(const RowView &rows, const SeqArgs &seq, int rows_total, float c,
                        const Workspace &ws, int kind, int dtype, cudaStream_t st);
+// Stochastic statistics plus every row's summary (top-p's first phase);
+// *seg gets the warp segment used (the summary's layout depends on it).
+int launch_stream_summary(const RowView &rows, int rows_total, float c, const Workspace &ws,
+                          int dtype, cudaStream_t st, long long *seg);
 // With top-p one CTA per row reduces the row's statistics, selects its
 // nucleus and takes the accept decisions (instead of the row kernel).
 int launch_topp_rows(const ToppArgs &a, int rows_total, int dtype, cudaStream_t st);

@@ -50,6 +50,11 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(const StreamArgs a) {
         if (KIND == 0) {
             warp_piece_ms<T>(rowp, lo, hi, a.c, m, s, fl);
             warp_reduce_ms(m, s, fl, a.c);
+        } else if (KIND == 2) {
+            uint32_t *sum = a.ws.sum + static_cast<size_t>(row) * a.ws.sum_stride +
+                            piece_sum_offset<T>(rowp, row, V, a.seg, w);
+            warp_piece_ms_sum<T>(rowp, lo, hi, a.c, sum, m, s, fl);
+            warp_reduce_ms(m, s, fl, a.c);
         } else {
             warp_piece_arg<T>(rowp, lo, hi, m, arg, fl);
             warp_reduce_arg(m, arg, fl);
@@ -84,11 +89,11 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(const StreamArgs a) {
                 const Partial *pp = a.ws.partial + static_cast<size_t>(row) * a.ws.pmax;
                 for (int i = lane; i < pieces; i += 32) {
                     const float m2 = __ldcg(&pp[i].m);
-                    if (KIND == 0) ms_combine(m, s, m2, __ldcg(&pp[i].s), a.c);
+                    if (KIND != 1) ms_combine(m, s, m2, __ldcg(&pp[i].s), a.c);
                     else arg_combine(m, arg, m2, __ldcg(&pp[i].arg));
                     fl |= __ldcg(&pp[i].flags);
                 }
-                if (KIND == 0) warp_reduce_ms(m, s, fl, a.c);
+                if (KIND != 1) warp_reduce_ms(m, s, fl, a.c);
                 else warp_reduce_arg(m, arg, fl);
                 if (lane == 0) write_row(dst, m, s, arg, fl);
                 row_done<T>(a.rows, a.seq, a.ws, a.c, row);
@@ -102,9 +107,10 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(const StreamArgs a) {
 
 template <typename T, int KIND>
 int launch_stream_t(const RowView &rows, const SeqArgs &seq, int rows_total, float c,
-                    const Workspace &ws, cudaStream_t st) {
+                    const Workspace &ws, cudaStream_t st, long long *seg_out = nullptr) {
     auto kernel = stream_kernel<T, KIND>;
-    const int ctas = resident_ctas(kernel, (sizeof(T) == 2 ? 2 : 0) + KIND);
+    const int ctas = resident_ctas(kernel, KIND == 2 ? (sizeof(T) == 2 ? 9 : 8)
+                                                     : (sizeof(T) == 2 ? 2 : 0) + KIND);
     if (ctas <= 0) return SPEC_ERR_CUDA;
     StreamArgs a;
     a.rows = rows;
@@ -118,6 +124,7 @@ int launch_stream_t(const RowView &rows, const SeqArgs &seq, int rows_total, flo
     a.ws = ws;
     const long long used = (a.total + a.seg - 1) / a.seg;
     const unsigned grid = static_cast<unsigned>((used + kWarps - 1) / kWarps);
+    if (seg_out) *seg_out = a.seg;
     kernel<<<grid, kThreads, 0, st>>>(a);
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
@@ -131,6 +138,15 @@ int launch_stream_rows(const RowView &rows, const SeqArgs &seq, int rows_total, 
                          : launch_stream_t<float, 1>(rows, seq, rows_total, c, ws, st);
     return kind == 0 ? launch_stream_t<uint16_t, 0>(rows, seq, rows_total, c, ws, st)
                      : launch_stream_t<uint16_t, 1>(rows, seq, rows_total, c, ws, st);
+}
+
+int launch_stream_summary(const RowView &rows, int rows_total, float c, const Workspace &ws,
+                          int dtype, cudaStream_t st, long long *seg) {
+    SeqArgs none = {};
+    none.work = kSeqNone;  // the decisions wait for the nucleus (topp.cu)
+    return dtype == SPEC_F32
+               ? launch_stream_t<float, 2>(rows, none, rows_total, c, ws, st, seg)
+               : launch_stream_t<uint16_t, 2>(rows, none, rows_total, c, ws, st, seg);
 }
 
 }  // namespace specv

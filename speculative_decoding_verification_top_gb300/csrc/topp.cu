@@ -9,32 +9,32 @@
 // mass from the top reaches top_p Z.  Masses are fixed-point integers
 // (2^-40 units) so every histogram sum is exact and order-independent.
 //
-// topp_kernel  one CTA per row.  It first reduces the row's max m and
-//              normaliser Z itself (8 warps, a split fixed by V), then:
-//   1. Tokens below c0 = m + T (ln((1 - top_p) Z / V) - ln 2) cannot be in
+// Two grids.  The statistics grid (rows.cu, kind 2) streams every row once
+// at full bandwidth: max m, normaliser Z, and the row's summary (the max
+// of every 32-logit group).  Then topp_kernel, one CTA per row:
+//   1. It gathers into shared memory every logit >= m - kToppTry T (a
+//      nucleus usually ends above it): the summary names the groups that
+//      reach it, and only those are read again (a few percent of the row).
+//   2. Tokens below c0 = m + T (ln((1 - top_p) Z / V) - ln 2) cannot be in
 //      the nucleus: all of them together carry < V e(c0) <= (1 - top_p) Z / 2.
-//   2. Pass A reads the row and histograms the mass of its logits >= y by
-//      value, uniformly over [y, m] (bins of keys would crowd the bulk of a
-//      row into a few bins: keys are log-spaced).  It first tries y = m -
-//      kToppTry T (a nucleus usually ends far above c0, and the logits in
-//      between are most of the work); if the mass of the logits >= y falls
-//      short of top_p Z it runs again with y = c0.  The bin where the mass
-//      from the top first reaches top_p Z holds lam.
-//      Pass A also keeps the logits it histogrammed in shared memory when
-//      they fit (kAList; a few percent of a peaked row).
-//   3. Pass B gathers the logits of that bin -- the same float arithmetic
-//      decides membership in both passes -- from that list (or, if it
-//      overflowed, from a second read of the row, which skips a 16-byte
-//      vector whose max is below the bin) and histograms them by key,
+//   3. Pass A histograms the mass of the gathered logits >= y by value,
+//      uniformly over [y, m] (bins of keys would crowd the bulk of a row
+//      into a few bins: keys are log-spaced), y = max(c0, m - kToppTry T);
+//      if that mass falls short of top_p Z it runs again with y = c0, from
+//      the row.  The bin where the mass from the top first reaches top_p Z
+//      holds lam.
+//   4. Pass B gathers the logits of that bin -- the same float arithmetic
+//      decides membership in both passes -- and histograms them by key,
 //      narrowing until one key is left: the largest key whose mass from the
 //      top reaches top_p Z.  (A bin holding more than kElemCap logits is
 //      narrowed from the row.)
 //   The row record gets lam and the kept mass; the warp that finishes a
 //   sequence's last row takes its accept decision.
 //   With top-k (a processor the target and the draft must share, "246
-//   Speculative Decoding", 6), the same select first runs by count: the
-//   K-th largest key, ties kept; top-p then runs on the kept set, its
-//   target top_p times the kept set's mass.
+//   Speculative Decoding", 6), step 1 gathers instead every logit >= a
+//   lower bound of the K-th largest (the K-th largest group max), the same
+//   select first runs by count: the K-th largest key, ties kept; top-p then
+//   runs on the kept set, its target top_p times the kept set's mass.
 
 #include "stream.cuh"
 
@@ -43,13 +43,7 @@ namespace {
 
 constexpr int kTpThreads = 256;  // one CTA per row
 constexpr int kTpWarps = kTpThreads / 32;
-constexpr int kAList = 3072;     // logits kept from pass A (shared memory)
-// Shared memory requested per CTA: more than the select needs, so that at
-// most three CTAs share an SM and the rows being selected (3 x 152 rows of
-// ~256 KB for bf16 V=128k) mostly stay in the 126 MB L2 between a CTA's
-// two reads of its row.  (Measured on c4: 2 per SM leaves HBM idle while
-// both CTAs of an SM select; 4 per SM spills registers and overflows L2.)
-constexpr int kToppSmem = 72 * 1024;
+constexpr int kAList = 3072;     // gathered logits held in shared memory
 
 struct SelShared {
     unsigned long long hist[kHistBins];
@@ -123,25 +117,36 @@ __device__ __forceinline__ void cta_clear(SelShared &sh) {
     __syncthreads();
 }
 
-struct ToppShared;
+constexpr int kMaxPieces = 64;   // pieces of one row the summary gather handles
+constexpr int kSumBuf = 6144;    // summary entries of one row staged in shared memory
+
 struct ToppShared {
     SelShared sel;
-    float alist[kAList];            // the logits pass A histogrammed (when they fit)
+    float alist[kAList];            // the gathered logits (when they fit)
     int aidx[kAList];               // ... and their indices in the row
-    float elems[kElemCap];          // the logits of the crossing bin (pass B from global)
-    float queue[kTpWarps][32 * 8];  // one vector slot of one warp (32 lanes x 8 logits)
-    int qidx[kTpWarps][32 * 8];     // ... and their indices in the row
-    int nidx[kElemCap];             // indices of the nucleus (list building)
-    float pm[kTpWarps], ps[kTpWarps];
-    uint32_t pf[kTpWarps];
+    union {
+        struct {
+            float elems[kElemCap];          // the logits of the crossing bin (pass B)
+            float queue[kTpWarps][32 * 8];  // one vector slot of one warp (32 lanes x 8 logits)
+            int qidx[kTpWarps][32 * 8];     // ... and their indices in the row
+            int nidx[kElemCap];             // indices of the nucleus (list building)
+        };
+        alignas(16) uint32_t sumbuf[kSumBuf];  // the row's summary while the list is gathered
+    };
+    // The row's pieces: [lo, hi), first vector a0, vectors nv, summary offset.
+    int pc_lo[kMaxPieces], pc_hi[kMaxPieces], pc_a0[kMaxPieces], pc_nv[kMaxPieces];
+    int pc_off[kMaxPieces + 1];
+    int n_pc, n_groups;
+    int sum_staged;                 // the summary is in sumbuf (else read from global)
+    unsigned int cnt8[kTpWarps];
     float m, Z;
     uint32_t flags;
-    uint32_t cmax;                  // running max of the row so far (ordered key)
     int n_alist, n_elems, n_nuc;
     unsigned int kmin, kmax;
     unsigned long long zacc;        // fixed-point mass of the top-k set
 };
-static_assert(sizeof(ToppShared) <= kToppSmem, "top-p shared memory");
+static_assert(sizeof(ToppShared) <= 100 * 1024, "top-p shared memory");
+static_assert(offsetof(ToppShared, sumbuf) % 16 == 0, "the staged summary is written as 16-byte vectors");
 
 // Every logit >= vmin of a row from global memory, calling `f(l, x)` on
 // each (x: its index in the row).
@@ -219,11 +224,33 @@ __device__ __forceinline__ void for_row(ToppShared &sh, const T *rowp, int V, fl
     }
 }
 
-// Append, for a whole warp, each lane's logits h[e] with bit e of `mask`
-// set (indices x0 + e) to the pass-A list: one shared atomic per warp.
-template <int N>
-__device__ __forceinline__ void alist_append(ToppShared &sh, uint32_t mask, const float (&h)[N],
-                                             int x0) {
+// One slot of *ctr per lane with `want`, one atomic per warp; the lane's
+// slot (meaningless without want).  Every lane of the warp calls it.
+__device__ __forceinline__ int warp_reserve(int *ctr, bool want) {
+    const unsigned bal = __ballot_sync(0xFFFFFFFFu, want);
+    if (!bal) return 0;
+    const int lane = threadIdx.x & 31, leader = __ffs(bal) - 1;
+    int base = 0;
+    if (lane == leader) base = atomicAdd(ctr, __popc(bal));
+    base = __shfl_sync(0xFFFFFFFFu, base, leader);
+    return base + __popc(bal & ((1u << lane) - 1u));
+}
+
+// Append logit l (index x) to the list where `want` (counted past kAList:
+// overflow).  Every lane of the warp calls it.
+__device__ __forceinline__ void alist_push(ToppShared &sh, bool want, float l, int x) {
+    const int pos = warp_reserve(&sh.n_alist, want);
+    if (want && pos < kAList) {
+        sh.alist[pos] = l;
+        sh.aidx[pos] = x;
+    }
+}
+
+// Append this lane's logits h[e] with bit e of `mask` set (indices x0 + e):
+// one atomic per warp.  Every lane of the warp calls it.
+template <int P>
+__device__ __forceinline__ void alist_push_mask(ToppShared &sh, uint32_t mask, const float (&h)[P],
+                                                int x0) {
     const int lane = threadIdx.x & 31;
     if (!__ballot_sync(0xFFFFFFFFu, mask != 0u)) return;
     const int cnt = __popc(mask);
@@ -233,13 +260,11 @@ __device__ __forceinline__ void alist_append(ToppShared &sh, uint32_t mask, cons
         const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
         if (lane >= o) incl += y;
     }
-    const int tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
     int base = 0;
-    if (lane == 31) base = atomicAdd(&sh.n_alist, tot);
-    base = __shfl_sync(0xFFFFFFFFu, base, 31);
-    int pos = base + incl - cnt;
+    if (lane == 31) base = atomicAdd(&sh.n_alist, incl);
+    int pos = __shfl_sync(0xFFFFFFFFu, base, 31) + incl - cnt;
 #pragma unroll
-    for (int e = 0; e < N; ++e)
+    for (int e = 0; e < P; ++e)
         if (mask & (1u << e)) {
             if (pos < kAList) {
                 sh.alist[pos] = h[e];
@@ -249,158 +274,207 @@ __device__ __forceinline__ void alist_append(ToppShared &sh, uint32_t mask, cons
         }
 }
 
-// Element e of a raw 16-byte vector as a float (no dynamic register
-// indexing: the word is picked by selects).
+// Row `row`'s pieces into sh.pc_* (the summary's layout).  Returns false
+// when the row has more than kMaxPieces pieces.
 template <typename T>
-__device__ __forceinline__ float elem_of(const uint4 &v, int e) {
-    if (Elem<T>::kPerVec == 4) {
-        const uint32_t w = e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
-        return __uint_as_float(w);
+__device__ bool stage_pieces(ToppShared &sh, const ToppArgs &a, int row, const T *rowp) {
+    const int tid = threadIdx.x, V = a.rows.V;
+    const long long rbase = static_cast<long long>(row) * V;
+    const long long wf = rbase / a.seg, wl = (rbase + V - 1) / a.seg;
+    const int np = static_cast<int>(wl - wf + 1);
+    if (np > kMaxPieces) return false;  // uniform
+    if (tid < np) {
+        int lo, hi;
+        piece_bounds(row, V, a.seg, wf + tid, lo, hi);
+        const Span<T> sp(rowp, lo, hi);
+        sh.pc_lo[tid] = lo;
+        sh.pc_hi[tid] = hi;
+        sh.pc_a0[tid] = sp.a0;
+        sh.pc_nv[tid] = sp.nvec;
     }
-    const int wi = e >> 1;
-    const uint32_t w = wi == 0 ? v.x : wi == 1 ? v.y : wi == 2 ? v.z : v.w;
-    return __uint_as_float((e & 1) ? (w & 0xFFFF0000u) : (w << 16));
+    __syncthreads();
+    if (tid == 0) {
+        int off = 0;
+        for (int i = 0; i < np; ++i) {
+            sh.pc_off[i] = off;
+            off += (sh.pc_nv[i] + kGroupVecs - 1) / kGroupVecs * 32;
+        }
+        sh.pc_off[np] = off;
+        sh.n_pc = np;
+    }
+    __syncthreads();
+    // The summary itself, when it fits (read as 16-byte vectors: piece
+    // offsets are multiples of 32 entries and rows start 128-byte aligned).
+    const int total = sh.pc_off[np];
+    const bool staged = total <= kSumBuf;
+    if (staged) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(a.ws.sum + static_cast<size_t>(row) *
+                                                                          a.ws.sum_stride);
+        uint4 *dst = reinterpret_cast<uint4 *>(sh.sumbuf);
+#pragma unroll 4
+        for (int v = tid; v < total / 4; v += kTpThreads) dst[v] = __ldcg(src + v);
+    }
+    if (tid == 0) sh.sum_staged = staged ? 1 : 0;
+    __syncthreads();
+    return true;
 }
 
-// alist_append for one batch of kBatch raw vectors per lane: bit u P + e of
-// `mask` is element e of vector u, at index x0 + u 32 P + e.  Each lane
-// walks only its set bits (typically none or one), so the cost follows the
-// candidates, not the batch size.
-template <typename T>
-__device__ __forceinline__ void alist_append_batch(ToppShared &sh, uint32_t mask,
-                                                   const uint4 (&q)[kBatch], int x0) {
-    static_assert(kBatch == 4, "vector selects below assume four vectors per lane");
-    constexpr int P = Elem<T>::kPerVec;
-    if (!mask) return;
-    // The list's order does not matter (every later use is a set or an
-    // integer sum): each lane reserves its own slots.
-    int pos = atomicAdd(&sh.n_alist, __popc(mask));
-    while (mask) {
-        const int i = __ffs(mask) - 1;
-        mask &= mask - 1u;
-        const int u = i / P, e = i - u * P;
-        const uint4 v = u == 0 ? q[0] : u == 1 ? q[1] : u == 2 ? q[2] : q[3];
-        if (pos < kAList) {
-            sh.alist[pos] = elem_of<T>(v, e);
-            sh.aidx[pos] = x0 + u * 32 * P + e;
+// Calls f(e, entry, valid) for every summary entry of the row (valid) and
+// for padding (not valid), every thread the same number of times, so that
+// f may use warp collectives; each thread's entries are loaded four at a
+// time with several loads in flight.  (Piece offsets are multiples of 32
+// entries and rows start 128-byte aligned.)
+template <typename F>
+__device__ __forceinline__ void for_entries(const ToppShared &sh, const ToppArgs &a, int row,
+                                            F &&f) {
+    const uint4 *src = sh.sum_staged
+                           ? reinterpret_cast<const uint4 *>(sh.sumbuf)
+                           : reinterpret_cast<const uint4 *>(a.ws.sum + static_cast<size_t>(row) *
+                                                                            a.ws.sum_stride);
+    const int nv = sh.pc_off[sh.n_pc] / 4;
+    constexpr int kUnroll = 4;
+    for (int base = 0; base < nv; base += kUnroll * kTpThreads) {  // uniform
+        uint4 w[kUnroll];
+#pragma unroll
+        for (int r = 0; r < kUnroll; ++r) {
+            const int v = base + r * kTpThreads + threadIdx.x;
+            w[r] = v >= nv ? make_uint4(0u, 0u, 0u, 0u) : sh.sum_staged ? src[v] : __ldcg(src + v);
         }
-        ++pos;
+#pragma unroll
+        for (int r = 0; r < kUnroll; ++r) {
+            const int v = base + r * kTpThreads + threadIdx.x;
+            const bool ok = v < nv;
+            f(4 * v, w[r].x, ok);
+            f(4 * v + 1, w[r].y, ok);
+            f(4 * v + 2, w[r].z, ok);
+            f(4 * v + 3, w[r].w, ok);
+        }
     }
 }
 
-// The float whose okey<float> is k.
-__device__ __forceinline__ float key_float(uint32_t k) {
-    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
-}
-
-// Statistics of the piece [lo, hi) of the row into this lane's (m_run,
-// s_run), as warp_piece_ms computes them, and meanwhile every logit >= (the
-// CTA's running max) - tryT appended to the pass-A list: the running max
-// never exceeds the row's max m, so every logit >= m - tryT is appended
-// (those the list can hold).
+// Every logit >= F of the row into the list: the groups whose summary max
+// reaches F are listed first, then read -- the vector holding the max, and
+// the group's other vectors only if their bound reaches F -- two groups per
+// thread and round, so that each thread's loads are in flight together;
+// and the pieces' ragged ends (not summarised).
 template <typename T>
-__device__ __forceinline__ void stats_capture(ToppShared &sh, const T *rowp, int lo, int hi,
-                                              float c, float tryT, float &m_run, float &s_run,
-                                              uint32_t &fl) {
+__device__ void gather_above(ToppShared &sh, const ToppArgs &a, int row, const T *rowp,
+                             float F) {
     constexpr int P = Elem<T>::kPerVec;
-    const int lane = threadIdx.x & 31;
-    const Span<T> sp(rowp, lo, hi);
-    auto scalar = [&](float l) {
-        if (l != l) {
-            fl |= kFlagNonFinite;
-            return;
-        }
-        if (l > m_run) {
-            s_run = __fmul_rn(s_run, ex2(__fmul_rn(__fsub_rn(m_run, l), c)));
-            m_run = l;
-        }
-        if (m_run != kNegInf)
-            s_run = __fadd_rn(s_run, ex2(__fmaf_rn(l, c, -__fmul_rn(m_run, c))));
-    };
-    // Threshold from this lane's and the CTA's running max (either is at
-    // most the row's max, so the floor never exceeds m - tryT).  A lane
-    // whose max grew publishes it with a shared atomic (rare once the row's
-    // top logits have been seen).
-    auto floor_now = [&](bool grew) {
-        if (grew && m_run > kNegInf) atomicMax(&sh.cmax, okey<float>(m_run));
-        const uint32_t ck = *reinterpret_cast<volatile uint32_t *>(&sh.cmax);
-        const float ref = ck ? fmaxf(m_run, key_float(ck)) : m_run;
-        return ref > kNegInf ? __fsub_rn(ref, tryT) : INFINITY;
-    };
-    // The ragged ends (< one vector each): counted, then appended if >= the floor.
-    auto edge = [&](int n0, int n1) {
-        float h[1] = {kNegInf};
-        if (lane < n1 - n0) {
-            h[0] = to_f32(rowp[n0 + lane]);
-            scalar(h[0]);
-        }
-        const float fl_now = floor_now(true);
-        alist_append<1>(sh, (h[0] >= fl_now && h[0] > kNegInf) ? 1u : 0u, h, n0 + lane);
-    };
-    edge(sp.e0, sp.a0);
-    const uint4 *vp = reinterpret_cast<const uint4 *>(rowp + sp.a0);
-    const uint4 neg = neg_inf_vec<T>();
-    constexpr int kStride = 32 * kBatch;
-    uint4 q[kBatch];
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) q[u] = lane + u * 32 < sp.nvec ? ld_stream(vp + lane + u * 32) : neg;
-    for (int v0 = 0; v0 < sp.nvec; v0 += kStride) {  // warp-uniform trip count
-        uint4 nq[kBatch];
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-            const int v = v0 + kStride + u * 32 + lane;
-            nq[u] = v < sp.nvec ? ld_stream(vp + v) : neg;
-        }
-        const float bm = batch_max<T>(q);
-        const bool nan = bm != bm;
-        bool grew = false;
-        if (nan) fl |= kFlagNonFinite;
-        else if (bm > m_run) {
-            s_run = __fmul_rn(s_run, ex2(__fmul_rn(__fsub_rn(m_run, bm), c)));
-            m_run = bm;
-            grew = true;
-        }
-        // Floor after this batch's max is counted (so the batch's own top
-        // logits are kept); one unpack feeds the sum and the capture mask.
-        const float thr = floor_now(grew);
-        const bool sum = !nan && m_run != kNegInf;
-        const float negmc = -__fmul_rn(m_run, c);
-        float2 acc = make_float2(0.0f, 0.0f);
-        float h[kBatch * P];
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-            float f[P];
-            unpack<T>(q[u], f);
-#pragma unroll
-            for (int e = 0; e < P; e += 2) {
-                const float2 x = fma2(make_float2(f[e], f[e + 1]), make_float2(c, c),
-                                      make_float2(negmc, negmc));
-                acc = add2(acc, make_float2(ex2(x.x), ex2(x.y)));
+    const int tid = threadIdx.x, np = sh.n_pc;
+    uint2 *glist = reinterpret_cast<uint2 *>(sh.sel.hist);  // (entry index, entry)
+    constexpr int kGList = static_cast<int>(sizeof(sh.sel.hist) / sizeof(uint2));
+    if (tid == 0) sh.n_groups = 0;
+    __syncthreads();
+    for_entries(sh, a, row, [&](int e, uint32_t en, bool ok) {
+        const bool want = ok && entry_max(en) >= F;
+        const int pos = warp_reserve(&sh.n_groups, want);
+        if (want && pos < kGList) glist[pos] = make_uint2(static_cast<uint32_t>(e), en);
+    });
+    __syncthreads();
+    const int ng = sh.n_groups;
+    if (ng > kGList) {
+        if (tid == 0) sh.n_alist = kAList + 1;  // too many: the row is read instead
+        return;
+    }
+    // Rounds: each thread loads one ragged-end logit (at most P - 1 before
+    // a0 and after a1 per piece) and kG groups, then tests them.
+    constexpr int kG = 2;
+    const int nr = np * 2 * (P - 1);
+    const int rounds = max((ng + kG * kTpThreads - 1) / (kG * kTpThreads),
+                           (nr + kTpThreads - 1) / kTpThreads);
+    for (int k = 0; k < rounds; ++k) {
+        float rl = kNegInf;
+        int rx = -1;
+        const int t = k * kTpThreads + tid;
+        if (t < nr) {
+            const int i = t / (2 * (P - 1)), r = t - i * 2 * (P - 1);
+            const int a0 = sh.pc_a0[i], a1 = a0 + sh.pc_nv[i] * P;
+            const int x = r < P - 1 ? sh.pc_lo[i] + r : a1 + (r - (P - 1));
+            if (r < P - 1 ? x < a0 : x < sh.pc_hi[i]) {
+                rl = to_f32(rowp[x]);
+                rx = x;
             }
-#pragma unroll
-            for (int e = 0; e < P; ++e) h[u * P + e] = f[e];
         }
-        if (sum) s_run = __fadd_rn(s_run, __fadd_rn(acc.x, acc.y));
-        // The capture mask only where this lane's batch reaches the floor:
-        // past the first batches of a peaked row almost none does.  (A
-        // finite floor excludes -inf logits; with no finite max yet the
-        // floor is +inf.)
-        uint32_t mask = 0u;
-        // Once the list has overflowed it is not used: stop filling it.
-        if (bm >= thr && *reinterpret_cast<volatile int *>(&sh.n_alist) <= kAList) {
+        uint4 q[kG][kBatch];
+        int x0[kG][kBatch];
 #pragma unroll
-            for (int i = 0; i < kBatch * P; ++i)
-                if (h[i] >= thr) mask |= 1u << i;
+        for (int r = 0; r < kG; ++r) {
+            const int g = (k * kG + r) * kTpThreads + tid;
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                q[r][u] = neg_inf_vec<T>();
+                x0[r][u] = 0;
+            }
+            if (g >= ng) continue;
+            const uint2 ge = glist[g];
+            const int e = static_cast<int>(ge.x);
+            int i = 0;
+            while (i + 1 < np && sh.pc_off[i + 1] <= e) ++i;
+            const int j = e - sh.pc_off[i], b = j >> 5, l = j & 31, nv = sh.pc_nv[i];
+            const int u1 = entry_vec(ge.y);
+            const bool all = entry_rest(ge.y) >= F;
+            const uint4 *vp = reinterpret_cast<const uint4 *>(rowp + sh.pc_a0[i]);
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int v = b * kGroupVecs + u * 32 + l;
+                x0[r][u] = sh.pc_a0[i] + v * P;
+                if (v < nv && (all || u == u1)) q[r][u] = __ldcg(vp + v);
+            }
         }
-        alist_append_batch<T>(sh, mask, q, sp.a0 + (v0 + lane) * P);
+        alist_push(sh, rx >= 0 && rl >= F, rl, rx);
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u) q[u] = nq[u];
+        for (int r = 0; r < kG; ++r)
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                float h[P];
+                unpack<T>(q[r][u], h);
+                uint32_t mask = 0u;
+#pragma unroll
+                for (int e2 = 0; e2 < P; ++e2)
+                    if (h[e2] >= F) mask |= 1u << e2;
+                alist_push_mask<P>(sh, mask, h, x0[r][u]);
+            }
     }
-    edge(sp.a1, sp.e1);
+}
+
+// A lower bound of the row's K-th largest logit from its summary: the K-th
+// largest group max (one bf16 step below it for fp32 logits, whose maxima
+// were rounded up) -- the largest 16-bit key k with at least K group keys
+// >= k, by bisection over the keys with block-wide counts.  Returns -inf
+// when the summary holds fewer than K finite groups (the ragged ends are
+// not summarised).
+template <typename T>
+__device__ float topk_floor(ToppShared &sh, const ToppArgs &a, int row, int K) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t kneg = sum_key(kNegInf);
+    auto count_ge = [&](uint32_t k) {
+        unsigned int c = 0u;
+        for_entries(sh, a, row, [&](int, uint32_t en, bool ok) { c += ok && (en >> 16) >= k; });
+        c = __reduce_add_sync(0xFFFFFFFFu, c);
+        if (lane == 0) sh.cnt8[warp] = c;
+        __syncthreads();
+        unsigned int tot = 0u;
+#pragma unroll
+        for (int w = 0; w < kTpWarps; ++w) tot += sh.cnt8[w];
+        __syncthreads();
+        return tot;
+    };
+    uint32_t lo = kneg + 1u, hi = 0xFFFFu;
+    if (count_ge(lo) < static_cast<unsigned int>(K)) return kNegInf;
+    while (lo < hi) {  // the largest k in [lo, hi] with count_ge(k) >= K
+        const uint32_t mid = (lo + hi + 1u) >> 1;
+        if (count_ge(mid) >= static_cast<unsigned int>(K)) lo = mid;
+        else hi = mid - 1u;
+    }
+    uint32_t key = lo;
+    if (sizeof(T) == 4) --key;  // one bf16 step below: every such group's max is above it
+    return key <= kneg ? kNegInf : sum_value(key);
 }
 
 // TOPK: the top-k select is compiled in (its own instantiation, so that the
-// top-p-only kernel keeps its registers).
+// top-p-only kernel keeps its registers).  The row's statistics and summary
+// come from the statistics grid (rows.cu), which ran before this one.
 template <typename T, bool TOPK>
 __global__ void __launch_bounds__(kTpThreads, 3) topp_kernel(const ToppArgs a) {
     // Let the dependent final-draw grid launch once every CTA of this grid
@@ -412,39 +486,27 @@ __global__ void __launch_bounds__(kTpThreads, 3) topp_kernel(const ToppArgs a) {
     RowRec *rec = a.ws.rows + row;
     const T *rowp = row_ptr<T>(a.rows, row);
     const float tryT = kToppTry * a.temperature;
-    {
-        // Row statistics: warp w reduces the w-th eighth of the row (a
-        // split fixed by V alone), combined in warp order; the logits near
-        // the running max are kept for the select.
-        const int V = a.rows.V, warp = tid >> 5;
-        const int per = ((V + kTpWarps - 1) / kTpWarps + 7) / 8 * 8;
-        const int lo = min(V, warp * per), hi = min(V, lo + per);
-        if (tid == 0) {
-            sh.n_alist = 0;
-            sh.cmax = 0u;
-        }
-        __syncthreads();
-        float pm = kNegInf, ps = 0.0f;
-        uint32_t pf = 0u;
-        stats_capture<T>(sh, rowp, lo, hi, a.c, tryT, pm, ps, pf);
-        warp_reduce_ms(pm, ps, pf, a.c);
-        if ((tid & 31) == 0) {
-            sh.pm[warp] = pm;
-            sh.ps[warp] = ps;
-            sh.pf[warp] = pf;
-        }
-        __syncthreads();
-        if (tid == 0) {
-            float mm = sh.pm[0], ss = sh.ps[0];
-            uint32_t ff = sh.pf[0];
-            for (int w = 1; w < kTpWarps; ++w) {
-                ms_combine(mm, ss, sh.pm[w], sh.ps[w], a.c);
-                ff |= sh.pf[w];
-            }
-            sh.m = mm;
-            sh.Z = ss;
-            sh.flags = row_flags(mm, ff);
-        }
+    const bool topk = TOPK && a.top_k > 0 && a.top_k < a.rows.V;
+    // The statistics grid's records and summaries: visible once it has
+    // completed.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (tid == 0) {
+        sh.m = __ldcg(&rec->m);
+        sh.Z = __ldcg(&rec->z_full);
+        sh.flags = __ldcg(&rec->flags);
+        sh.n_alist = 0;
+    }
+    __syncthreads();
+    // The list: every logit >= gfloor -- m - tryT (a nucleus usually ends
+    // above it), or with top-k a lower bound of the K-th largest logit
+    // (everything top-k keeps, and so everything top-p then sees).
+    float gfloor = __fsub_rn(sh.m, tryT);
+    if (sh.flags == 0u) {
+        bool ok = stage_pieces<T>(sh, a, row, rowp);
+        if (ok && topk) gfloor = topk_floor<T>(sh, a, row, a.top_k);
+        ok = ok && gfloor > kNegInf;
+        if (ok) gather_above<T>(sh, a, row, rowp, gfloor);
+        else if (tid == 0) sh.n_alist = kAList + 1;  // no usable bound: the row is read instead
         __syncthreads();
     }
     const float m = sh.m;
@@ -457,11 +519,16 @@ __global__ void __launch_bounds__(kTpThreads, 3) topp_kernel(const ToppArgs a) {
         const float c = a.c;
         const float negmc = -__fmul_rn(m, c);
         __syncthreads();
-        // What the list holds: every logit >= list_lo (the statistics pass
-        // kept every logit >= m - tryT, unless the list overflowed).
+        // What the list holds: every logit >= list_lo (unless it overflowed).
         const float tryfloor = m - tryT;
-        float list_lo = sh.n_alist <= kAList ? tryfloor : INFINITY;
+        float list_lo = sh.n_alist <= kAList ? gfloor : INFINITY;
         uint32_t kfloor = 0u;  // keys below it are not kept (top-k; 0: none)
+        // The smallest logit value kfloor keeps (-inf: none).
+        auto kval = [&]() {
+            return kfloor == 0u ? kNegInf : key_float(sizeof(T) == 2 ? kfloor << 16 : kfloor);
+        };
+        // The list holds every kept logit >= lo.
+        auto in_list = [&](float lo) { return fmaxf(lo, kval()) >= list_lo; };
         float span = 0.0f, inv = 0.0f;
         auto vbin = [&](float l) {
             return min(static_cast<int>(__fmul_rn(__fsub_rn(m, l), inv)), kHistBins - 1);
@@ -493,7 +560,7 @@ __global__ void __launch_bounds__(kTpThreads, 3) topp_kernel(const ToppArgs a) {
                 span = __fsub_rn(m, lo);
                 inv = span > 0.0f ? static_cast<float>(kHistBins) / span : 0.0f;
                 cta_clear(sh.sel);
-                if (lo >= list_lo) {
+                if (in_list(lo)) {
                     const int na0 = sh.n_alist;
                     for (int i = tid; i < na0; i += kTpThreads) {
                         const float l = sh.alist[i];
@@ -547,9 +614,22 @@ __global__ void __launch_bounds__(kTpThreads, 3) topp_kernel(const ToppArgs a) {
                     atomicMax(&sh.kmax, okey<T>(l));
                 }
             };
-            if (lo >= list_lo) {
+            if (in_list(lo)) {
                 const int na = sh.n_alist;
-                for (int i = tid; i < na; i += kTpThreads) take(sh.alist[i], 0);
+                for (int i0 = 0; i0 < na; i0 += kTpThreads) {  // uniform
+                    const int i = i0 + tid;
+                    const float l = i < na ? sh.alist[i] : kNegInf;
+                    const bool in = i < na && in_b0(l);
+                    const int pos = warp_reserve(&sh.n_elems, in);
+                    if (in && pos < kElemCap) sh.elems[pos] = l;
+                    const uint32_t kl = __reduce_min_sync(0xFFFFFFFFu, in ? okey<T>(l) : 0xFFFFFFFFu);
+                    const uint32_t kh = __reduce_max_sync(0xFFFFFFFFu, in ? okey<T>(l) : 0u);
+                    const bool any = __any_sync(0xFFFFFFFFu, in);
+                    if ((tid & 31) == 0 && any) {
+                        atomicMin(&sh.kmin, kl);
+                        atomicMax(&sh.kmax, kh);
+                    }
+                }
             } else {
                 for_row<T>(sh, rowp, V, vmin, take);
             }
@@ -598,36 +678,36 @@ __global__ void __launch_bounds__(kTpThreads, 3) topp_kernel(const ToppArgs a) {
         float zsel = Z;          // mass the top-p target is relative to
         float final_lo = tryfloor;  // every kept logit is >= it
         bool have_lam = false;
-        if (TOPK && a.top_k > 0 && a.top_k < V) {
-            // Top-k: the K-th largest key by count, over the logits near
-            // the max first (the list), then over windows of the row 1.5
-            // times wider each (a window that first holds K logits then holds
-            // few more, so they mostly fit the list for the passes after);
-            // beyond the widest (4608 T below the max) a logit's weight
-            // 2^((l - m) c) is zero in fp32.
-            // If the list overflowed, the row is dense near its max and the
-            // K-th largest usually lies well inside tryT: the windows start
-            // at tryT / 4 (from the row) and double up to tryT first.
+        if (topk) {
+            // Top-k: the K-th largest key by count.  The list holds every
+            // logit >= a lower bound of it: one window.  Else (the list
+            // overflowed) over windows of the row, from tryT / 4 below the
+            // max, doubling to tryT, then 1.5 times wider each (a window
+            // that first holds K logits then holds few more, so they mostly
+            // fit the list for the passes after); beyond the widest (4608 T
+            // below the max) a logit's weight 2^((l - m) c) is zero in fp32.
             float los[11];
             int nlo = 0;
-            if (list_lo == INFINITY) {
+            if (list_lo != INFINITY) {
+                los[nlo++] = list_lo;
+            } else {
                 los[nlo++] = __fsub_rn(m, __fmul_rn(0.25f, tryT));
                 los[nlo++] = __fsub_rn(m, __fmul_rn(0.5f, tryT));
+                los[nlo++] = tryfloor;
+                float wdt = tryT;
+                for (int i = 0; i < 7; ++i) {
+                    wdt = __fmul_rn(wdt, 1.5f);
+                    los[nlo++] = __fsub_rn(m, wdt);
+                }
+                los[nlo++] = __fsub_rn(m, __fmul_rn(512.0f, tryT));
             }
-            los[nlo++] = tryfloor;
-            float wdt = tryT;
-            for (int i = 0; i < 7; ++i) {
-                wdt = __fmul_rn(wdt, 1.5f);
-                los[nlo++] = __fsub_rn(m, wdt);
-            }
-            los[nlo++] = __fsub_rn(m, __fmul_rn(512.0f, tryT));
             const uint32_t tau = select(true, static_cast<unsigned long long>(a.top_k), los, nlo);
             const float lo_k = sel_lo;
             kfloor = tau;
             // Fixed-point mass of the kept set (keys >= tau, all >= lo_k).
             if (tid == 0) sh.zacc = 0ull;
             __syncthreads();
-            if (lo_k >= list_lo) {
+            if (in_list(lo_k)) {
                 const int na = sh.n_alist;
                 for (int i = tid; i < na; i += kTpThreads) {
                     const float l = sh.alist[i];
@@ -676,16 +756,17 @@ __global__ void __launch_bounds__(kTpThreads, 3) topp_kernel(const ToppArgs a) {
             __syncthreads();
             const int na2 = sh.n_alist;
             // The list holds every kept logit (all are >= final_lo).
-            const bool covers = na2 <= kAList && final_lo >= list_lo;
+            const bool covers = na2 <= kAList && in_list(final_lo);
             if (covers) {
-                for (int i = tid; i < na2; i += kTpThreads)
-                    if (okey<T>(sh.alist[i]) >= lam) {
-                        const int pos = atomicAdd(&sh.n_nuc, 1);
-                        if (pos < kElemCap) {
-                            sh.elems[pos] = sh.alist[i];
-                            sh.nidx[pos] = sh.aidx[i];
-                        }
+                for (int i0 = 0; i0 < na2; i0 += kTpThreads) {  // uniform
+                    const int i = i0 + tid;
+                    const bool keep = i < na2 && okey<T>(sh.alist[i]) >= lam;
+                    const int pos = warp_reserve(&sh.n_nuc, keep);
+                    if (keep && pos < kElemCap) {
+                        sh.elems[pos] = sh.alist[i];
+                        sh.nidx[pos] = sh.aidx[i];
                     }
+                }
             }
             __syncthreads();
             const int nn = sh.n_nuc;
@@ -792,7 +873,7 @@ bool topp_smem_ok(K kernel, int slot) {
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return false;
     if (__atomic_load_n(&done[dev][slot], __ATOMIC_RELAXED)) return true;
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kToppSmem) != cudaSuccess)
+                             sizeof(ToppShared)) != cudaSuccess)
         return false;
     __atomic_store_n(&done[dev][slot], 1, __ATOMIC_RELAXED);
     return true;
@@ -800,26 +881,39 @@ bool topp_smem_ok(K kernel, int slot) {
 
 template <typename T, bool TOPK>
 int launch_topp_t(const ToppArgs &a, int rows_total, cudaStream_t st) {
-    if (!topp_smem_ok(topp_kernel<T, TOPK>, (sizeof(T) == 2 ? 1 : 0) + (TOPK ? 2 : 0)))
-        return SPEC_ERR_CUDA;
+    auto kernel = topp_kernel<T, TOPK>;
+    if (!topp_smem_ok(kernel, (sizeof(T) == 2 ? 1 : 0) + (TOPK ? 2 : 0))) return SPEC_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(rows_total));
     cfg.blockDim = dim3(kTpThreads);
-    cfg.dynamicSmemBytes = kToppSmem;
-    cfg.stream = st;  // first kernel of a call: plain stream order
-    return cudaLaunchKernelEx(&cfg, topp_kernel<T, TOPK>, a) == cudaSuccess ? SPEC_OK
-                                                                             : SPEC_ERR_CUDA;
+    cfg.dynamicSmemBytes = sizeof(ToppShared);
+    cfg.stream = st;
+    // Launched behind the statistics grid, which it waits for.
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, a) == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+// The statistics grid (max, normaliser and summary of every row), then
+// one select CTA per row.
+template <typename T>
+int launch_topp_two(const ToppArgs &in, int rows_total, cudaStream_t st) {
+    ToppArgs a = in;
+    const int rc = launch_stream_summary(a.rows, rows_total, a.c, a.ws,
+                                         sizeof(T) == 2 ? SPEC_BF16 : SPEC_F32, st, &a.seg);
+    if (rc != SPEC_OK) return rc;
+    return a.top_k > 0 ? launch_topp_t<T, true>(a, rows_total, st)
+                       : launch_topp_t<T, false>(a, rows_total, st);
 }
 
 }  // namespace
 
 int launch_topp_rows(const ToppArgs &a, int rows_total, int dtype, cudaStream_t st) {
-    const bool topk = a.top_k > 0;
-    if (dtype == SPEC_F32)
-        return topk ? launch_topp_t<float, true>(a, rows_total, st)
-                    : launch_topp_t<float, false>(a, rows_total, st);
-    return topk ? launch_topp_t<uint16_t, true>(a, rows_total, st)
-                : launch_topp_t<uint16_t, false>(a, rows_total, st);
+    return dtype == SPEC_F32 ? launch_topp_two<float>(a, rows_total, st)
+                             : launch_topp_two<uint16_t>(a, rows_total, st);
 }
 
 }  // namespace specv
