@@ -29,7 +29,7 @@ LIB_PATH = os.path.join(_PKG, "libspecverify.so")
 CSRC = os.path.join(_PKG, "csrc")
 SOURCES = [os.path.join(CSRC, f)
            for f in ("api.cu", "rows.cu", "topp.cu", "final.cu", "noalloc.cu",
-                     "accept.cu", "treemask.cu", "treesample.cu")]
+                     "accept.cu", "treemask.cu", "treesample.cu", "select.cu")]
 HEADERS = [os.path.join(CSRC, f) for f in ("common.cuh", "stream.cuh", "draw.cuh")]
 INCLUDE = os.path.join(_ROOT, "include")
 HEADER = os.path.join(INCLUDE, "spec_verify.h")

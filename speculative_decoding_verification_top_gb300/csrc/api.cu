@@ -43,6 +43,7 @@ size_t carve(void *base, int B, int rows_per_seq, int V, Workspace *ws, bool cha
     const size_t pairs = chain ? static_cast<size_t>(B) * ((rows_per_seq - 1) / 2) : 0;
     char *accq = take(chain ? (pairs + 2) * sizeof(uint32_t) : 0);
     char *sum = take(capture ? rows * sum_stride_for(V) * sizeof(uint32_t) : 0);
+    char *defer = take(capture ? rows * sizeof(uint32_t) : 0);
     if (ws) {
         ws->err = reinterpret_cast<uint32_t *>(err);
         ws->row_ctr = reinterpret_cast<uint32_t *>(row_ctr);
@@ -57,6 +58,7 @@ size_t carve(void *base, int B, int rows_per_seq, int V, Workspace *ws, bool cha
         ws->accq = reinterpret_cast<uint32_t *>(accq);
         ws->sum = reinterpret_cast<uint32_t *>(sum);
         ws->sum_stride = sum_stride_for(V);
+        ws->defer = reinterpret_cast<uint32_t *>(defer);
         ws->pmax = pmax;
     }
     return off;

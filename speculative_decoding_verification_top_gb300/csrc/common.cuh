@@ -79,6 +79,7 @@ struct Workspace {
     uint32_t *accq;        // acceptance queue: [0] length, [1] CTA arrivals, then [B k] pair ids
     uint32_t *sum;         // [rows, sum_stride] row summaries, one entry per group (top-p / top-k)
     int sum_stride;        // summary entries per row
+    uint32_t *defer;       // [rows] 1: the row is left to topp_kernel (reset by it)
     int pmax;              // partial slots per row
 };
 
@@ -729,6 +730,7 @@ struct ToppArgs {
     float c, temperature, top_p;
     int top_k;         // keep the top_k largest logits and their ties first (0: off)
     long long seg;     // warp segment of the statistics grid (the summaries' layout)
+    int rows_total;    // rows of the grid
     Workspace ws;
 };
 
@@ -826,6 +828,9 @@ int launch_stream_summary(const RowView &rows, int rows_total, float c, const Wo
 // With top-p one CTA per row reduces the row's statistics, selects its
 // nucleus and takes the accept decisions (instead of the row kernel).
 int launch_topp_rows(const ToppArgs &a, int rows_total, int dtype, cudaStream_t st);
+// The per-row select, one warp per row (select.cu); rows it defers are
+// taken by topp_kernel.
+int launch_select_warp(const ToppArgs &a, int dtype, cudaStream_t st);
 // The final kernel is launched as a programmatic dependent of the row kernel.
 int launch_final(const FinalArgs &a, int dtype, cudaStream_t st);
 int launch_tree(const TreeArgs &a, cudaStream_t st);

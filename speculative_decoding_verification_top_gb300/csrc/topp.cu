@@ -44,6 +44,13 @@ namespace {
 constexpr int kTpThreads = 256;  // one CTA per row
 constexpr int kTpWarps = kTpThreads / 32;
 constexpr int kAList = 3072;     // gathered logits held in shared memory
+// Shared memory requested per fused CTA: more than the select needs, so that
+// at most three CTAs share an SM and the rows being selected (3 x 152 rows
+// of ~256 KB for bf16 V=128k) mostly stay in the 126 MB L2 between a CTA's
+// two reads of its row.  (Measured on c4: 2 per SM leaves HBM idle while
+// both CTAs of an SM select; 4 per SM spills registers and overflows L2;
+// 6 CTAs of 128 threads per SM, one wave, takes 1.7x as long.)
+constexpr int kToppSmem = 72 * 1024;
 
 struct SelShared {
     unsigned long long hist[kHistBins];
@@ -136,6 +143,9 @@ struct ToppShared {
     // The row's pieces: [lo, hi), first vector a0, vectors nv, summary offset.
     int pc_lo[kMaxPieces], pc_hi[kMaxPieces], pc_a0[kMaxPieces], pc_nv[kMaxPieces];
     int pc_off[kMaxPieces + 1];
+    float pm[kTpWarps], ps[kTpWarps];  // per-warp statistics (fused)
+    uint32_t pf[kTpWarps];
+    uint32_t cmax;                  // running max of the row so far (ordered key; fused)
     int n_pc, n_groups;
     int sum_staged;                 // the summary is in sumbuf (else read from global)
     unsigned int cnt8[kTpWarps];
@@ -145,7 +155,7 @@ struct ToppShared {
     unsigned int kmin, kmax;
     unsigned long long zacc;        // fixed-point mass of the top-k set
 };
-static_assert(sizeof(ToppShared) <= 100 * 1024, "top-p shared memory");
+static_assert(sizeof(ToppShared) <= kToppSmem, "top-p shared memory");
 static_assert(offsetof(ToppShared, sumbuf) % 16 == 0, "the staged summary is written as 16-byte vectors");
 
 // Every logit >= vmin of a row from global memory, calling `f(l, x)` on
@@ -222,6 +232,186 @@ __device__ __forceinline__ void for_row(ToppShared &sh, const T *rowp, int V, fl
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) q[u] = nq[u];
     }
+}
+
+// Append, for a whole warp, each lane's logits h[e] with bit e of `mask`
+// set (indices x0 + e) to the pass-A list: one shared atomic per warp.
+template <int N>
+__device__ __forceinline__ void alist_append(ToppShared &sh, uint32_t mask, const float (&h)[N],
+                                             int x0) {
+    const int lane = threadIdx.x & 31;
+    if (!__ballot_sync(0xFFFFFFFFu, mask != 0u)) return;
+    const int cnt = __popc(mask);
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    const int tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    int base = 0;
+    if (lane == 31) base = atomicAdd(&sh.n_alist, tot);
+    base = __shfl_sync(0xFFFFFFFFu, base, 31);
+    int pos = base + incl - cnt;
+#pragma unroll
+    for (int e = 0; e < N; ++e)
+        if (mask & (1u << e)) {
+            if (pos < kAList) {
+                sh.alist[pos] = h[e];
+                sh.aidx[pos] = x0 + e;
+            }
+            ++pos;
+        }
+}
+
+// Element e of a raw 16-byte vector as a float (no dynamic register
+// indexing: the word is picked by selects).
+template <typename T>
+__device__ __forceinline__ float elem_of(const uint4 &v, int e) {
+    if (Elem<T>::kPerVec == 4) {
+        const uint32_t w = e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
+        return __uint_as_float(w);
+    }
+    const int wi = e >> 1;
+    const uint32_t w = wi == 0 ? v.x : wi == 1 ? v.y : wi == 2 ? v.z : v.w;
+    return __uint_as_float((e & 1) ? (w & 0xFFFF0000u) : (w << 16));
+}
+
+// alist_append for one batch of kBatch raw vectors per lane: bit u P + e of
+// `mask` is element e of vector u, at index x0 + u 32 P + e.  Each lane
+// walks only its set bits (typically none or one), so the cost follows the
+// candidates, not the batch size.
+template <typename T>
+__device__ __forceinline__ void alist_append_batch(ToppShared &sh, uint32_t mask,
+                                                   const uint4 (&q)[kBatch], int x0) {
+    static_assert(kBatch == 4, "vector selects below assume four vectors per lane");
+    constexpr int P = Elem<T>::kPerVec;
+    if (!mask) return;
+    // The list's order does not matter (every later use is a set or an
+    // integer sum): each lane reserves its own slots.
+    int pos = atomicAdd(&sh.n_alist, __popc(mask));
+    while (mask) {
+        const int i = __ffs(mask) - 1;
+        mask &= mask - 1u;
+        const int u = i / P, e = i - u * P;
+        const uint4 v = u == 0 ? q[0] : u == 1 ? q[1] : u == 2 ? q[2] : q[3];
+        if (pos < kAList) {
+            sh.alist[pos] = elem_of<T>(v, e);
+            sh.aidx[pos] = x0 + u * 32 * P + e;
+        }
+        ++pos;
+    }
+}
+
+// The float whose okey<float> is k.
+__device__ __forceinline__ float key_float(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// Statistics of the piece [lo, hi) of the row into this lane's (m_run,
+// s_run), as warp_piece_ms computes them, and meanwhile every logit >= (the
+// CTA's running max) - tryT appended to the pass-A list: the running max
+// never exceeds the row's max m, so every logit >= m - tryT is appended
+// (those the list can hold).
+template <typename T>
+__device__ __forceinline__ void stats_capture(ToppShared &sh, const T *rowp, int lo, int hi,
+                                              float c, float tryT, float &m_run, float &s_run,
+                                              uint32_t &fl) {
+    constexpr int P = Elem<T>::kPerVec;
+    const int lane = threadIdx.x & 31;
+    const Span<T> sp(rowp, lo, hi);
+    auto scalar = [&](float l) {
+        if (l != l) {
+            fl |= kFlagNonFinite;
+            return;
+        }
+        if (l > m_run) {
+            s_run = __fmul_rn(s_run, ex2(__fmul_rn(__fsub_rn(m_run, l), c)));
+            m_run = l;
+        }
+        if (m_run != kNegInf)
+            s_run = __fadd_rn(s_run, ex2(__fmaf_rn(l, c, -__fmul_rn(m_run, c))));
+    };
+    // Threshold from this lane's and the CTA's running max (either is at
+    // most the row's max, so the floor never exceeds m - tryT).  A lane
+    // whose max grew publishes it with a shared atomic (rare once the row's
+    // top logits have been seen).
+    auto floor_now = [&](bool grew) {
+        if (grew && m_run > kNegInf) atomicMax(&sh.cmax, okey<float>(m_run));
+        const uint32_t ck = *reinterpret_cast<volatile uint32_t *>(&sh.cmax);
+        const float ref = ck ? fmaxf(m_run, key_float(ck)) : m_run;
+        return ref > kNegInf ? __fsub_rn(ref, tryT) : INFINITY;
+    };
+    // The ragged ends (< one vector each): counted, then appended if >= the floor.
+    auto edge = [&](int n0, int n1) {
+        float h[1] = {kNegInf};
+        if (lane < n1 - n0) {
+            h[0] = to_f32(rowp[n0 + lane]);
+            scalar(h[0]);
+        }
+        const float fl_now = floor_now(true);
+        alist_append<1>(sh, (h[0] >= fl_now && h[0] > kNegInf) ? 1u : 0u, h, n0 + lane);
+    };
+    edge(sp.e0, sp.a0);
+    const uint4 *vp = reinterpret_cast<const uint4 *>(rowp + sp.a0);
+    const uint4 neg = neg_inf_vec<T>();
+    constexpr int kStride = 32 * kBatch;
+    uint4 q[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) q[u] = lane + u * 32 < sp.nvec ? ld_stream(vp + lane + u * 32) : neg;
+    for (int v0 = 0; v0 < sp.nvec; v0 += kStride) {  // warp-uniform trip count
+        uint4 nq[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int v = v0 + kStride + u * 32 + lane;
+            nq[u] = v < sp.nvec ? ld_stream(vp + v) : neg;
+        }
+        const float bm = batch_max<T>(q);
+        const bool nan = bm != bm;
+        bool grew = false;
+        if (nan) fl |= kFlagNonFinite;
+        else if (bm > m_run) {
+            s_run = __fmul_rn(s_run, ex2(__fmul_rn(__fsub_rn(m_run, bm), c)));
+            m_run = bm;
+            grew = true;
+        }
+        // Floor after this batch's max is counted (so the batch's own top
+        // logits are kept); one unpack feeds the sum and the capture mask.
+        const float thr = floor_now(grew);
+        const bool sum = !nan && m_run != kNegInf;
+        const float negmc = -__fmul_rn(m_run, c);
+        float2 acc = make_float2(0.0f, 0.0f);
+        float h[kBatch * P];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            float f[P];
+            unpack<T>(q[u], f);
+#pragma unroll
+            for (int e = 0; e < P; e += 2) {
+                const float2 x = fma2(make_float2(f[e], f[e + 1]), make_float2(c, c),
+                                      make_float2(negmc, negmc));
+                acc = add2(acc, make_float2(ex2(x.x), ex2(x.y)));
+            }
+#pragma unroll
+            for (int e = 0; e < P; ++e) h[u * P + e] = f[e];
+        }
+        if (sum) s_run = __fadd_rn(s_run, __fadd_rn(acc.x, acc.y));
+        // The capture mask only where this lane's batch reaches the floor:
+        // past the first batches of a peaked row almost none does.  (A
+        // finite floor excludes -inf logits; with no finite max yet the
+        // floor is +inf.)
+        uint32_t mask = 0u;
+        // Once the list has overflowed it is not used: stop filling it.
+        if (bm >= thr && *reinterpret_cast<volatile int *>(&sh.n_alist) <= kAList) {
+#pragma unroll
+            for (int i = 0; i < kBatch * P; ++i)
+                if (h[i] >= thr) mask |= 1u << i;
+        }
+        alist_append_batch<T>(sh, mask, q, sp.a0 + (v0 + lane) * P);
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) q[u] = nq[u];
+    }
+    edge(sp.a1, sp.e1);
 }
 
 // One slot of *ctr per lane with `want`, one atomic per warp; the lane's
@@ -473,9 +663,12 @@ __device__ float topk_floor(ToppShared &sh, const ToppArgs &a, int row, int K) {
 }
 
 // TOPK: the top-k select is compiled in (its own instantiation, so that the
-// top-p-only kernel keeps its registers).  The row's statistics and summary
-// come from the statistics grid (rows.cu), which ran before this one.
-template <typename T, bool TOPK>
+// top-p-only kernel keeps its registers).  FUSED: the CTA streams its row
+// itself (statistics, and the logits near the running max into the list),
+// the first kernel of a call; else it takes the rows the warp select
+// (select.cu) deferred, with their statistics and summaries from the
+// statistics grid (rows.cu), and every other CTA exits.
+template <typename T, bool TOPK, bool FUSED>
 __global__ void __launch_bounds__(kTpThreads, 3) topp_kernel(const ToppArgs a) {
     // Let the dependent final-draw grid launch once every CTA of this grid
     // has started (it waits for this grid's completion before reading).
@@ -487,27 +680,74 @@ __global__ void __launch_bounds__(kTpThreads, 3) topp_kernel(const ToppArgs a) {
     const T *rowp = row_ptr<T>(a.rows, row);
     const float tryT = kToppTry * a.temperature;
     const bool topk = TOPK && a.top_k > 0 && a.top_k < a.rows.V;
-    // The statistics grid's records and summaries: visible once it has
-    // completed.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (tid == 0) {
-        sh.m = __ldcg(&rec->m);
-        sh.Z = __ldcg(&rec->z_full);
-        sh.flags = __ldcg(&rec->flags);
-        sh.n_alist = 0;
-    }
-    __syncthreads();
     // The list: every logit >= gfloor -- m - tryT (a nucleus usually ends
-    // above it), or with top-k a lower bound of the K-th largest logit
-    // (everything top-k keeps, and so everything top-p then sees).
-    float gfloor = __fsub_rn(sh.m, tryT);
-    if (sh.flags == 0u) {
-        bool ok = stage_pieces<T>(sh, a, row, rowp);
-        if (ok && topk) gfloor = topk_floor<T>(sh, a, row, a.top_k);
-        ok = ok && gfloor > kNegInf;
-        if (ok) gather_above<T>(sh, a, row, rowp, gfloor);
-        else if (tid == 0) sh.n_alist = kAList + 1;  // no usable bound: the row is read instead
+    // above it), or with top-k (not fused) a lower bound of the K-th largest
+    // logit (everything top-k keeps, and so everything top-p then sees).
+    float gfloor;
+    if (FUSED) {
+        // Row statistics: warp w reduces the w-th eighth of the row (a
+        // split fixed by V alone), combined in warp order; the logits near
+        // the running max are kept for the select.
+        const int V = a.rows.V, warp = tid >> 5;
+        const int per = ((V + kTpWarps - 1) / kTpWarps + 7) / 8 * 8;
+        const int lo = min(V, warp * per), hi = min(V, lo + per);
+        if (tid == 0) {
+            sh.n_alist = 0;
+            sh.cmax = 0u;
+        }
         __syncthreads();
+        float pm = kNegInf, ps = 0.0f;
+        uint32_t pf = 0u;
+        stats_capture<T>(sh, rowp, lo, hi, a.c, tryT, pm, ps, pf);
+        warp_reduce_ms(pm, ps, pf, a.c);
+        if ((tid & 31) == 0) {
+            sh.pm[warp] = pm;
+            sh.ps[warp] = ps;
+            sh.pf[warp] = pf;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            float mm = sh.pm[0], ss = sh.ps[0];
+            uint32_t ff = sh.pf[0];
+            for (int w = 1; w < kTpWarps; ++w) {
+                ms_combine(mm, ss, sh.pm[w], sh.ps[w], a.c);
+                ff |= sh.pf[w];
+            }
+            sh.m = mm;
+            sh.Z = ss;
+            sh.flags = row_flags(mm, ff);
+        }
+        __syncthreads();
+        // The statistics pass kept every logit >= m - tryT, unless the list
+        // overflowed.
+        gfloor = __fsub_rn(sh.m, tryT);
+    } else {
+        // The warp select's deferrals (and before it the statistics grid's
+        // records and summaries): visible once it has completed.
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        if (tid == 0) {
+            sh.flags = __ldcg(&a.ws.defer[row]);
+            if (sh.flags) a.ws.defer[row] = 0u;  // this CTA is its only reader
+        }
+        __syncthreads();
+        if (!sh.flags) return;  // taken by the warp select
+        __syncthreads();
+        if (tid == 0) {
+            sh.m = __ldcg(&rec->m);
+            sh.Z = __ldcg(&rec->z_full);
+            sh.flags = __ldcg(&rec->flags);
+            sh.n_alist = 0;
+        }
+        __syncthreads();
+        gfloor = __fsub_rn(sh.m, tryT);
+        if (sh.flags == 0u) {
+            bool ok = stage_pieces<T>(sh, a, row, rowp);
+            if (ok && topk) gfloor = topk_floor<T>(sh, a, row, a.top_k);
+            ok = ok && gfloor > kNegInf;
+            if (ok) gather_above<T>(sh, a, row, rowp, gfloor);
+            else if (tid == 0) sh.n_alist = kAList + 1;  // no usable bound: the row is read instead
+            __syncthreads();
+        }
     }
     const float m = sh.m;
     const float Z = sh.Z;
@@ -868,45 +1108,54 @@ __global__ void __launch_bounds__(kTpThreads, 3) topp_kernel(const ToppArgs a) {
 template <typename K>
 bool topp_smem_ok(K kernel, int slot) {
     constexpr int kMaxDev = 64;
-    static int done[kMaxDev][4];
+    static int done[kMaxDev][8];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return false;
     if (__atomic_load_n(&done[dev][slot], __ATOMIC_RELAXED)) return true;
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             sizeof(ToppShared)) != cudaSuccess)
+                             kToppSmem) != cudaSuccess)
         return false;
     __atomic_store_n(&done[dev][slot], 1, __ATOMIC_RELAXED);
     return true;
 }
 
-template <typename T, bool TOPK>
+template <typename T, bool TOPK, bool FUSED>
 int launch_topp_t(const ToppArgs &a, int rows_total, cudaStream_t st) {
-    auto kernel = topp_kernel<T, TOPK>;
-    if (!topp_smem_ok(kernel, (sizeof(T) == 2 ? 1 : 0) + (TOPK ? 2 : 0))) return SPEC_ERR_CUDA;
+    auto kernel = topp_kernel<T, TOPK, FUSED>;
+    if (!topp_smem_ok(kernel, (sizeof(T) == 2 ? 1 : 0) + (TOPK ? 2 : 0) + (FUSED ? 4 : 0)))
+        return SPEC_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(rows_total));
     cfg.blockDim = dim3(kTpThreads);
-    cfg.dynamicSmemBytes = sizeof(ToppShared);
+    cfg.dynamicSmemBytes = FUSED ? kToppSmem : sizeof(ToppShared);
     cfg.stream = st;
-    // Launched behind the statistics grid, which it waits for.
+    // Not fused: launched behind the warp select, which it waits for.
+    // Fused: the first kernel of a call, in plain stream order.
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.attrs = FUSED ? nullptr : attr;
+    cfg.numAttrs = FUSED ? 0 : 1;
     return cudaLaunchKernelEx(&cfg, kernel, a) == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
-// The statistics grid (max, normaliser and summary of every row), then
-// one select CTA per row.
+// Top-p alone: the fused kernel, one CTA per row.  With top-k: the
+// statistics grid (max, normaliser and summary of every row), the warp
+// select, then the CTAs of the rows it deferred.  (Measured on the 128-row
+// bf16 workloads: the fused kernel is the faster for top-p, where the
+// logits it keeps while streaming are all the select needs; for top-k the
+// summary finds the K largest without a second read of dense rows.)
 template <typename T>
 int launch_topp_two(const ToppArgs &in, int rows_total, cudaStream_t st) {
     ToppArgs a = in;
-    const int rc = launch_stream_summary(a.rows, rows_total, a.c, a.ws,
-                                         sizeof(T) == 2 ? SPEC_BF16 : SPEC_F32, st, &a.seg);
+    a.rows_total = rows_total;
+    if (a.top_k <= 0) return launch_topp_t<T, false, true>(a, rows_total, st);
+    const int dtype = sizeof(T) == 2 ? SPEC_BF16 : SPEC_F32;
+    int rc = launch_stream_summary(a.rows, rows_total, a.c, a.ws, dtype, st, &a.seg);
     if (rc != SPEC_OK) return rc;
-    return a.top_k > 0 ? launch_topp_t<T, true>(a, rows_total, st)
-                       : launch_topp_t<T, false>(a, rows_total, st);
+    rc = launch_select_warp(a, dtype, st);
+    if (rc != SPEC_OK) return rc;
+    return launch_topp_t<T, true, false>(a, rows_total, st);
 }
 
 }  // namespace
