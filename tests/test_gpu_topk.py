@@ -111,6 +111,31 @@ def test_k_beyond_the_near_max_list(K):
     check(wl, K, t, n, max_mismatch_frac=0.5)
 
 
+@pytest.mark.parametrize("K", [128, 129])
+def test_at_the_warp_select_limit(K):
+    """K at the largest the warp-per-row select takes (128) and one above
+    (the row goes to the per-row CTA select, which bounds the K-th largest
+    from the row summary itself)."""
+    wl = workloads.c4(B=6)
+    topk_tokens(wl, K, 11)
+    t, n, ws = run(wl, K)
+    check(wl, K, t, n, max_mismatch_frac=0.5)
+    assert sv.last_error(ws) == 0
+
+
+@pytest.mark.parametrize("V", [100003, 200003])
+def test_rows_of_many_pieces(V):
+    """Few rows of a large vocabulary: the statistics grid's warp segments
+    are at their shortest, so a row spans 50 to 100 pieces -- more than the
+    warp select maps, and at V = 200003 more than the CTA select stages (it
+    then searches the row itself)."""
+    wl = _small_chain(2, 1, V, workloads.BF16, 0.8, 0.9, seed=V)
+    topk_tokens(wl, 50, 7)
+    t, n, ws = run(wl, 50)
+    check(wl, 50, t, n, max_mismatch_frac=0.5)
+    assert sv.last_error(ws) == 0
+
+
 def test_flat_rows_overflow_the_list():
     rng = np.random.default_rng(6)
     B, k, V = 6, 2, 20011
