@@ -96,8 +96,8 @@ __device__ __forceinline__ void st_keep(uint32_t *p, uint32_t v, uint64_t pol) {
 
 // warp_piece_ms, and the piece's summary: entry b 32 + lane of `sum` gets
 // sum_entry of this lane's kBatch vectors of batch b, a store of 4 bytes
-// per lane and batch.
-template <typename T>
+// per lane and batch (SMEM: `sum` is in shared memory).
+template <typename T, bool SMEM = false>
 __device__ __forceinline__ void warp_piece_ms_sum(const T *rowp, int lo, int hi, float c,
                                                   uint32_t *sum, float &m_run, float &s_run,
                                                   uint32_t &fl) {
@@ -136,7 +136,8 @@ __device__ __forceinline__ void warp_piece_ms_sum(const T *rowp, int lo, int hi,
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) mu[u] = batch_max1<T>(q[u]);
         const float bm = max_nan(max_nan(mu[0], mu[1]), max_nan(mu[2], mu[3]));
-        st_keep(sl, sum_entry(mu), keep);
+        if (SMEM) *sl = sum_entry(mu);
+        else st_keep(sl, sum_entry(mu), keep);
         if (bm != bm) {
             fl |= kFlagNonFinite;
         } else {

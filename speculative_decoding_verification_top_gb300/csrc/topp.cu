@@ -686,19 +686,46 @@ __global__ void __launch_bounds__(kTpThreads, 3) topp_kernel(const ToppArgs a) {
     float gfloor;
     if (FUSED) {
         // Row statistics: warp w reduces the w-th eighth of the row (a
-        // split fixed by V alone), combined in warp order; the logits near
-        // the running max are kept for the select.
+        // split fixed by V alone), combined in warp order.  Meanwhile, when
+        // the row's summary fits the staging buffer, each warp writes its
+        // piece's summary there (a store per lane and batch) and the
+        // near-max groups are gathered after, from L2 (the CTA has just
+        // streamed its row); else the logits near the running max are
+        // kept as they stream by.
         const int V = a.rows.V, warp = tid >> 5;
         const int per = ((V + kTpWarps - 1) / kTpWarps + 7) / 8 * 8;
         const int lo = min(V, warp * per), hi = min(V, lo + per);
+        int off = 0, total = 0;
+        for (int w = 0; w < kTpWarps; ++w) {
+            const int l2 = min(V, w * per), h2 = min(V, l2 + per);
+            const int g = piece_groups<T>(rowp, l2, h2);
+            off += w < warp ? g : 0;
+            total += g;
+        }
+        const bool summ = total <= kSumBuf;
         if (tid == 0) {
             sh.n_alist = 0;
             sh.cmax = 0u;
         }
+        if (tid < kTpWarps) {
+            const int l2 = min(V, tid * per), h2 = min(V, l2 + per);
+            const Span<T> sp(rowp, l2, h2);
+            sh.pc_lo[tid] = l2;
+            sh.pc_hi[tid] = h2;
+            sh.pc_a0[tid] = sp.a0;
+            sh.pc_nv[tid] = sp.nvec;
+        }
         __syncthreads();
         float pm = kNegInf, ps = 0.0f;
         uint32_t pf = 0u;
-        stats_capture<T>(sh, rowp, lo, hi, a.c, tryT, pm, ps, pf);
+        if (summ) warp_piece_ms_sum<T, true>(rowp, lo, hi, a.c, sh.sumbuf + off, pm, ps, pf);
+        else stats_capture<T>(sh, rowp, lo, hi, a.c, tryT, pm, ps, pf);
+        if ((tid & 31) == 0) sh.pc_off[warp] = off;
+        if (tid == 0) {
+            sh.pc_off[kTpWarps] = total;
+            sh.n_pc = kTpWarps;
+            sh.sum_staged = 1;
+        }
         warp_reduce_ms(pm, ps, pf, a.c);
         if ((tid & 31) == 0) {
             sh.pm[warp] = pm;
@@ -718,9 +745,12 @@ __global__ void __launch_bounds__(kTpThreads, 3) topp_kernel(const ToppArgs a) {
             sh.flags = row_flags(mm, ff);
         }
         __syncthreads();
-        // The statistics pass kept every logit >= m - tryT, unless the list
-        // overflowed.
+        // The list: every logit >= m - tryT (unless it overflowed).
         gfloor = __fsub_rn(sh.m, tryT);
+        if (summ && sh.flags == 0u) {
+            gather_above<T>(sh, a, row, rowp, gfloor);
+            __syncthreads();
+        }
     } else {
         // The warp select's deferrals (and before it the statistics grid's
         // records and summaries): visible once it has completed.
