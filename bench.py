@@ -27,6 +27,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import subprocess
 import sys
 import tempfile
@@ -171,25 +172,37 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def source_code_hash(paths):
+    """First 16 hex digits of the sha256 of the sources' code: comments,
+    blank lines and trailing spaces removed, so that a comment edit does not
+    count as a kernel change."""
+    h = hashlib.sha256()
+    for path in paths:
+        text = open(path).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for line in text.splitlines():
+            line = re.sub(r"//.*$", "", line).rstrip()
+            if line:
+                h.update(line.encode() + b"\n")
+    return h.hexdigest()[:16]
+
+
 def profiled_traffic(kernel, config):
     """dram bytes per launch of `kernel` from its committed ncu summary, if
-    that was taken on this workload and on the current kernel source (else
+    that was taken on this workload and on the current kernel code (else
     None)."""
     summary, sources = PROFILES[kernel]
     try:
         text = open(summary).read()
-        h = hashlib.sha256()
-        for path in sources:
-            h.update(open(path, "rb").read())
-        src = h.hexdigest()[:16]
+        src = source_code_hash(sources)
     except OSError:
         return None
     fields = {}
     for line in text.splitlines():
-        if line.split(":", 1)[0] in ("traffic_bytes_per_launch", "source_sha256_16", "workload"):
+        if line.split(":", 1)[0] in ("traffic_bytes_per_launch", "source_code_sha256_16", "workload"):
             k, v = line.split(":", 1)
             fields[k.strip()] = v.strip()
-    if (fields.get("source_sha256_16") != src or fields.get("workload") != config
+    if (fields.get("source_code_sha256_16") != src or fields.get("workload") != config
             or "traffic_bytes_per_launch" not in fields):
         return None
     return float(fields["traffic_bytes_per_launch"])

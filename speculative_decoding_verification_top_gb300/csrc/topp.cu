@@ -9,15 +9,21 @@
 // mass from the top reaches top_p Z.  Masses are fixed-point integers
 // (2^-40 units) so every histogram sum is exact and order-independent.
 //
-// Two grids.  The statistics grid (rows.cu, kind 2) streams every row once
-// at full bandwidth: max m, normaliser Z, and the row's summary (the max
-// of every 32-logit group).  Then topp_kernel, one CTA per row:
-//   1. It gathers into shared memory every logit >= m - kToppTry T (a
-//      nucleus usually ends above it): the summary names the groups that
-//      reach it, and only those are read again (a few percent of the row).
+// topp_kernel, one CTA per row:
+//   1. Statistics and the list.  Fused (top-p alone, the call's first
+//      kernel): the CTA streams its row -- max m, normaliser Z, and per
+//      warp the summary of its piece in shared memory (the max of every
+//      group of logits one lane reduces in one batch) -- then reads again
+//      the groups within kToppTry T of m (a nucleus usually ends above
+//      m - kToppTry T) into a shared list; rows too long for the shared
+//      summary keep instead the logits near the running max as they
+//      stream by.  Not fused (top-k: rows the warp select of select.cu
+//      deferred): m, Z and the summary come from the statistics grid
+//      (rows.cu, kind 2), and the list is every logit >= a lower bound of
+//      the K-th largest (the K-th largest group max).
 //   2. Tokens below c0 = m + T (ln((1 - top_p) Z / V) - ln 2) cannot be in
 //      the nucleus: all of them together carry < V e(c0) <= (1 - top_p) Z / 2.
-//   3. Pass A histograms the mass of the gathered logits >= y by value,
+//   3. Pass A histograms the mass of the listed logits >= y by value,
 //      uniformly over [y, m] (bins of keys would crowd the bulk of a row
 //      into a few bins: keys are log-spaced), y = max(c0, m - kToppTry T);
 //      if that mass falls short of top_p Z it runs again with y = c0, from
@@ -31,10 +37,9 @@
 //   The row record gets lam and the kept mass; the warp that finishes a
 //   sequence's last row takes its accept decision.
 //   With top-k (a processor the target and the draft must share, "246
-//   Speculative Decoding", 6), step 1 gathers instead every logit >= a
-//   lower bound of the K-th largest (the K-th largest group max), the same
-//   select first runs by count: the K-th largest key, ties kept; top-p then
-//   runs on the kept set, its target top_p times the kept set's mass.
+//   Speculative Decoding", 6) the same select first runs by count: the
+//   K-th largest key, ties kept; top-p then runs on the kept set, its
+//   target top_p times the kept set's mass.
 
 #include "stream.cuh"
 
