@@ -3,17 +3,18 @@
 // The thresholds are defined in topp.cu's header ("3.5 Speculative
 // Decoding", "Notation"; top-k: "246 Speculative Decoding", 6): lam is the
 // largest key whose fixed-point mass from the top reaches top_p Z (ties of
-// lam kept), tau the K-th largest key by count.  Both are plain step
-// functions of the key, so a bisection over the key space with exact
-// integer counts or masses finds exactly the key the histogram select of
-// topp.cu finds.
+// lam kept), tau the K-th largest key by count.  Both are step functions
+// of the key with exact integer weights, so a value histogram (monotone
+// bins) followed by a bisection over the keys of the crossing bin finds
+// exactly the key the histogram select of topp.cu finds.
 //
 // select_warp_kernel  one warp per row, no block barriers, one wave:
 //   1. the row's summary (rows.cu) names the groups whose max reaches the
 //      floor F -- m - kToppTry T, or with top-k a lower bound of the K-th
 //      largest logit (the K-th largest of the group maxima each lane kept)
 //      -- and only those vectors are read again (mostly one per group);
-//   2. bisection for tau (count) and lam (mass) over the gathered logits;
+//   2. tau (count) and lam (mass) over the gathered logits: a 256-bin value
+//      histogram, then a bisection inside the crossing bin;
 //   3. for a target row, its nucleus list ranked by index with the draft
 //      value at each index;
 //   4. the row record, and the sequence's decision when this was its last
@@ -42,7 +43,7 @@ static_assert(kSwBuckets + kNucCap <= kSwList, "the ranking scratch reuses lx");
 struct SwWarp {
     float lv[kSwList];      // gathered logits
     int lx[kSwList];        // ... and their indices in the row
-    uint32_t gl[kSwGroups]; // selected groups: piece << 27 | u1 << 25 | all << 24 | entry;
+    uint32_t gl[kSwGroups]; // selected groups: u1 << 25 | all << 24 | entry (in the row);
                             // then the crossing bin's logits; then the nucleus,
                             // (index, logit bits) pairs
     unsigned long long hist[kSwBins];  // the threshold select's histogram
