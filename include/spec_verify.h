@@ -93,8 +93,11 @@ enum {
 
 /*
  * Workspace bytes needed by spec_verify_sample for batch B, draft length k
- * and vocabulary V (either mode, either dtype).  Returns SPEC_OK or
- * SPEC_ERR_NULL / SPEC_ERR_SHAPE.
+ * and vocabulary V (either mode, either dtype), and by every other chain
+ * call on the same shape (top-k included).  The top-k calls' row summaries
+ * are laid out last, so calls without top-k also accept a workspace that
+ * stops before them (the size of the other parts, ~16 KB per target row
+ * plus small records).  Returns SPEC_OK or SPEC_ERR_NULL / SPEC_ERR_SHAPE.
  */
 int spec_verify_workspace_size(int B, int k, int V, size_t *bytes);
 
@@ -339,8 +342,9 @@ int spec_verify_tree_mask(const int32_t *parents, const int32_t *pos0, int B, in
  * the library's own device image, held by every GPU that loads the library
  * until the process exits.  It calls no allocator.
  *   - Same arguments and results as spec_verify_sample, without the
- *     workspace.  Batches whose workspace (spec_verify_workspace_size)
- *     exceeds 4 MiB are rejected with SPEC_ERR_WORKSPACE.
+ *     workspace.  Batches whose workspace without the top-k part (see
+ *     spec_verify_workspace_size) exceeds 4 MiB are rejected with
+ *     SPEC_ERR_WORKSPACE.
  *   - Each call zero-fills the part of the scratch it uses on `stream`
  *     first.  All calls on a device share the one array: calls whose work
  *     overlaps on the GPU race and give wrong results; order them.

@@ -19,6 +19,8 @@ int pmax_for(int V) { return (V + kMinSeg - 1) / kMinSeg + 2; }
 // Carve the workspace; returns the bytes needed (base may be null).
 // `chain`: a chain call (rows_per_seq = 2k+1), which also needs the top-p
 // nucleus lists of its B (k+1) target rows; a tree call does not.
+// `capture`: the row summaries and deferral flags of the top-k path, laid
+// out last, so that calls without top-k need only what comes before.
 size_t carve(void *base, int B, int rows_per_seq, int V, Workspace *ws, bool chain,
              bool capture) {
     const size_t rows = static_cast<size_t>(B) * rows_per_seq;
@@ -110,7 +112,8 @@ int plan_chain(const void *target_logits, const void *draft_logits, const int32_
         !aligned(draft_tokens, 4) || (stoch && !aligned(uniforms, 4)) ||
         !aligned(out_tokens, 4) || !aligned(out_num_accepted, 4) || !aligned(workspace, 16))
         return SPEC_ERR_ALIGN;
-    if (workspace_bytes < carve(nullptr, B, 2 * k + 1, V, nullptr, true, true))
+    const bool topk_on = stoch && top_k > 0 && top_k < V;
+    if (workspace_bytes < carve(nullptr, B, 2 * k + 1, V, nullptr, true, topk_on))
         return SPEC_ERR_WORKSPACE;
 
     plan->stoch = stoch;
@@ -122,7 +125,7 @@ int plan_chain(const void *target_logits, const void *draft_logits, const int32_
     plan->use_topp = stoch && (top_p < 1.0f || plan->top_k > 0);
     plan->c = static_cast<float>(1.4426950408889634 / static_cast<double>(plan->temperature));
     plan->st = reinterpret_cast<cudaStream_t>(stream);
-    carve(workspace, B, 2 * k + 1, V, &plan->ws, true, true);
+    carve(workspace, B, 2 * k + 1, V, &plan->ws, true, topk_on);
 
     RowView &rv = plan->rows;
     rv.target = target_logits;
@@ -183,6 +186,11 @@ int launch_chain_finish(const ChainPlan &p) {
 }
 
 }  // namespace
+
+size_t chain_workspace_bytes(int B, int k, int V, bool topk) {
+    return carve(nullptr, B, 2 * k + 1, V, nullptr, true, topk);
+}
+
 }  // namespace specv
 
 using namespace specv;
@@ -453,11 +461,11 @@ SPEC_EXPORT int spec_verify_intermediates(const void *workspace, size_t workspac
                                           spec_stream_t stream) {
     if (!workspace) return SPEC_ERR_NULL;
     if (!chain_sizes_ok(B, k, V)) return SPEC_ERR_SHAPE;
-    if (workspace_bytes < carve(nullptr, B, 2 * k + 1, V, nullptr, true, true))
+    if (workspace_bytes < carve(nullptr, B, 2 * k + 1, V, nullptr, true, false))
         return SPEC_ERR_WORKSPACE;
     if (B == 0) return SPEC_OK;
     Workspace ws;
-    carve(const_cast<void *>(workspace), B, 2 * k + 1, V, &ws, true, true);
+    carve(const_cast<void *>(workspace), B, 2 * k + 1, V, &ws, true, false);
     return launch_intermediates(ws, B, k, P, Q, Z, S, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -477,10 +485,11 @@ SPEC_EXPORT int spec_verify_acceptance(const void *target_logits, const void *dr
     if (!aligned(target_logits, esz) || !aligned(draft_logits, esz) || !aligned(out_beta, 4) ||
         (out_tv && !aligned(out_tv, 4)) || !aligned(workspace, 16))
         return SPEC_ERR_ALIGN;
-    if (workspace_bytes < carve(nullptr, B, 2 * k + 1, V, nullptr, true, true))
+    const bool topk_on = top_k > 0 && top_k < V;
+    if (workspace_bytes < carve(nullptr, B, 2 * k + 1, V, nullptr, true, topk_on))
         return SPEC_ERR_WORKSPACE;
     AcceptArgs a;
-    carve(workspace, B, 2 * k + 1, V, &a.ws, true, true);
+    carve(workspace, B, 2 * k + 1, V, &a.ws, true, topk_on);
     a.rows.target = target_logits;
     a.rows.draft = draft_logits;
     a.rows.V = V;

@@ -28,6 +28,11 @@
 
 #define SPEC_EXPORT extern "C" __attribute__((visibility("default")))
 
+namespace specv {
+// Workspace bytes a chain call needs (api.cu), with or without top-k.
+size_t chain_workspace_bytes(int B, int k, int V, bool topk);
+}  // namespace specv
+
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;  // 4 MiB per device
@@ -64,6 +69,7 @@ SPEC_EXPORT int spec_verify_sample_noalloc(const void *target_logits, const void
     size_t need = 0;
     const int rc = spec_verify_workspace_size(B, k, V, &need);
     if (rc != SPEC_OK) return rc;
+    need = specv::chain_workspace_bytes(B, k, V, false);  // no top-k: not the summaries
     if (need > kNoAllocScratchBytes) return SPEC_ERR_WORKSPACE;  // batch too large for the scratch
     if (B == 0) return SPEC_OK;
     void *scratch = scratch_on_current_device();
