@@ -17,8 +17,12 @@
 //                 finishes a sequence's last row (a second arrival count)
 //                 takes that sequence's accept decision -- or, in greedy
 //                 mode, emits its tokens.
-//                 With top-p the decisions wait for the nucleus: the
-//                 top-p kernel (topp.cu) takes them.
+//                 Kinds: 0 stochastic statistics, 1 first argmax, 2
+//                 stochastic statistics and the row summaries (the max of
+//                 each lane's batch of vectors, stream.cuh) that the top-k
+//                 select reads (select.cu, topp.cu).  With top-p or top-k
+//                 the decisions wait for the nucleus: the select kernels
+//                 take them.
 
 #include "stream.cuh"
 
