@@ -186,6 +186,18 @@ def test_ragged_vocab(V, dtype):
     np.testing.assert_array_equal(gt, gref["tokens"])
 
 
+@pytest.mark.parametrize("V,dtype", [(131071, workloads.F32), (262147, workloads.BF16)])
+def test_top_p_long_rows(V, dtype):
+    """Rows too long for the fused top-p kernel's shared-memory summary
+    (fp32 V = 131071, bf16 V = 262147): it keeps the logits near the running
+    max as they stream by instead."""
+    wl = _small_chain(3, 2, V, dtype, 0.8, 0.9, seed=V)
+    t, n, ws = run_gpu(wl)
+    ref = run_oracle(wl)
+    flags = check_stochastic(wl, t, n, ref, max_mismatch_frac=0.5)
+    check_intermediates(wl, ws, ref, flags)
+
+
 @pytest.mark.parametrize("dtype", [workloads.F32, workloads.BF16])
 def test_unaligned_base(dtype):
     """Logit arrays that start one element past a 16-byte boundary."""
