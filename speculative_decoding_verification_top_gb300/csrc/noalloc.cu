@@ -20,7 +20,11 @@
 //
 // Set-up: the first call on a device, with that device current, looks up
 // the array's device address (cudaGetSymbolAddress) and caches it for that
-// device.  Make that first call before any stream capture begins.
+// device.  Make that first call before any stream capture begins.  The
+// cached address belongs to the device's primary context, which the CUDA
+// runtime keeps for the life of the process: a caller that destroys it
+// (cudaDeviceReset) must not use this entry point on that device again in
+// the same process, since the cache would still hold the old address.
 
 #include <mutex>
 
@@ -69,9 +73,14 @@ SPEC_EXPORT int spec_verify_sample_noalloc(const void *target_logits, const void
     size_t need = 0;
     const int rc = spec_verify_workspace_size(B, k, V, &need);
     if (rc != SPEC_OK) return rc;
+    // B = 0: spec_verify_sample checks the mode, dtype and sizes, enqueues
+    // nothing and touches no pointer.
+    if (B == 0)
+        return spec_verify_sample(target_logits, draft_logits, draft_tokens, uniforms, B, k, V,
+                                  temperature, top_p, mode, dtype, out_tokens, out_num_accepted,
+                                  nullptr, 0, stream);
     need = specv::chain_workspace_bytes(B, k, V, false);  // no top-k: not the summaries
     if (need > kNoAllocScratchBytes) return SPEC_ERR_WORKSPACE;  // batch too large for the scratch
-    if (B == 0) return SPEC_OK;
     void *scratch = scratch_on_current_device();
     if (!scratch) return SPEC_ERR_CUDA;
     // Validate every other argument without enqueueing anything:
