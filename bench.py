@@ -44,13 +44,38 @@ PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 7900.0
 _CSRC = os.path.join(ROOT, "speculative_decoding_verification_top_gb300", "csrc")
+_INCLUDE = os.path.join(ROOT, "include")
+
+
+def include_closure(tu):
+    """The translation unit `tu` and every file it reaches through
+    `#include "..."` (looked up beside the including file, then in csrc/ and
+    include/), in a fixed order: the unit first, then the rest sorted."""
+    seen, todo = [], [os.path.abspath(tu)]
+    while todo:
+        f = todo.pop()
+        if f in seen:
+            continue
+        seen.append(f)
+        for name in re.findall(r'^\s*#\s*include\s+"([^"]+)"', open(f).read(), flags=re.M):
+            for d in (os.path.dirname(f), _CSRC, _INCLUDE):
+                cand = os.path.abspath(os.path.join(d, name))
+                if os.path.exists(cand):
+                    todo.append(cand)
+                    break
+            else:
+                raise FileNotFoundError("%s includes %s, which was not found" % (f, name))
+    return [seen[0]] + sorted(seen[1:])
+
+
 # The committed ncu summary of each row-phase kernel, and the sources whose
-# hash it was taken on (its traffic is reported only while they match).
+# hash it was taken on: the kernel's translation unit and everything it
+# includes (its traffic is reported only while they match).
 PROFILES = {
     "stream_kernel": (os.path.join(ROOT, "profiles", "stream_kernel_c3.md"),
-                      [os.path.join(_CSRC, f) for f in ("common.cuh", "stream.cuh", "rows.cu")]),
+                      include_closure(os.path.join(_CSRC, "rows.cu"))),
     "topp_kernel": (os.path.join(ROOT, "profiles", "topp_kernel_c4.md"),
-                    [os.path.join(_CSRC, f) for f in ("common.cuh", "topp.cu")]),
+                    include_closure(os.path.join(_CSRC, "topp.cu"))),
 }
 
 
@@ -59,11 +84,16 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--config", default="c3", choices=["c2", "c3", "c4", "c5"])
+    ap.add_argument("--config", default="c3", choices=["c1", "c2", "c3", "c4", "c5"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
-                    help="budget of the CPU-oracle baseline sample")
+                    help="budget of the CPU-oracle baseline sample (each of one core, all cores)")
+    ap.add_argument("--no-blocks", action="store_true",
+                    help="only the headline workload (no c1/c2/c4/c5 blocks after it)")
+    ap.add_argument("--quick", action="store_true",
+                    help="a short run for profiling: no blocks, no load around the timed "
+                         "calls, 50 individually timed calls")
     return ap.parse_args()
 
 
@@ -271,8 +301,8 @@ class Job:
         self.sv.spec_verify_sample_rows(*self.chain_args(i))
 
 
-def device_launch_ms(launch, n, stream, chunk=100):
-    """Mean device time of launch(i), i < n, each bracketed by CUDA events on
+def call_times_ms(launch, n, stream, chunk=100):
+    """Device time of each launch(i), i < n, bracketed by CUDA events on
     `stream`.  Each chunk of launches is queued behind a ~25 ms device-side
     sleep, so the host is far ahead when they run: the events time the
     kernels back to back, not the host's launch latency."""
@@ -289,7 +319,51 @@ def device_launch_ms(launch, n, stream, chunk=100):
             b.record(stream)
         torch.cuda.synchronize()
         times += [a.elapsed_time(b) for a, b in evs]
-    return float(np.mean(times))
+    return times
+
+
+def device_launch_ms(launch, n, stream, chunk=100):
+    """Mean of call_times_ms."""
+    return float(np.mean(call_times_ms(launch, n, stream, chunk)))
+
+
+def per_call(times_ms):
+    """Best, median and mean of per-call device times, in microseconds."""
+    t = np.asarray(times_ms) * 1e3
+    return {"n": int(t.size), "best_us": round(float(t.min()), 2),
+            "median_us": round(float(np.median(t)), 2), "mean_us": round(float(t.mean()), 2)}
+
+
+def soak(job, seconds, step0=0):
+    """Whole calls back to back for about `seconds` (untimed load that keeps
+    the clocks where the timed calls run them)."""
+    import torch
+    if seconds <= 0:
+        return step0
+    t0, i = time.perf_counter(), step0
+    while time.perf_counter() - t0 < seconds:
+        for _ in range(50):
+            job.step(i)
+            i += 1
+        torch.cuda.synchronize()
+    return i
+
+
+def pinned_h2d_gbs(dev, nbytes=256 << 20, reps=8):
+    """Host-to-device copy rate from pinned memory: one large copy repeated,
+    timed with CUDA events (the link's rate for the e2e leg's copies)."""
+    import torch
+    h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    d.copy_(h, non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        d.copy_(h, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    return round(nbytes * reps / (e0.elapsed_time(e1) * 1e-3) / 1e9, 1)
 
 
 def timed_device(job, steps, warmup, world, kernel_launches=500):
@@ -535,30 +609,166 @@ def timed_e2e(job, steps):
     return e0.elapsed_time(e1), wall * 1e3, h2d, d2h
 
 
-def cpu_baseline(wl, mode, seconds):
-    """The fp64 oracle, as it stands, on one host core over a bounded sample:
-    whole sequences of the same workload, round-robin, until `seconds`."""
+def _oracle_sequence(arrs, mode, b, meta):
+    """One whole sequence b of a workload through the fp64 oracle; returns
+    the logit bytes it read."""
+    import oracle
+    sl = slice(b, b + 1)
+    if mode == "tree":
+        oracle.verify_tree(arrs["target"][sl], arrs["parents"], arrs["node_tokens"][sl], meta["D"])
+    else:
+        oracle.verify_sample(arrs["target"][sl], arrs["draft"][sl], arrs["draft_tokens"][sl],
+                             arrs["uniforms"][sl], T=meta["T"], top_p=meta["top_p"])
+    return meta["bytes_per_seq"]
+
+
+def _oracle_worker(task):
+    """A spawned worker: sequences b0, b0+1, ... (mod B), n of them, from
+    the workload's arrays memory-mapped from `folder`."""
+    folder, mode, meta, b0, n = task
+    arrs = {k: np.load(os.path.join(folder, k + ".npy"), mmap_mode="r") for k in meta["arrays"]}
+    done = 0
+    for i in range(n):
+        done += _oracle_sequence(arrs, mode, (b0 + i) % meta["B"], meta)
+    return done
+
+
+def _host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(wl, mode, seconds, all_cores=True):
+    """The fp64 oracle, as it stands, on the host cores over bounded
+    samples of the same workload: whole sequences, round-robin over the
+    batch.  First one core for `seconds`; then, if all_cores, every core at
+    once (one spawned process per core, each running sequences from the
+    workload's arrays memory-mapped from a temporary folder) for about
+    `seconds` more."""
     import oracle
     oracle.build()
+    if mode == "tree":
+        arrs = {"target": wl.target, "parents": wl.parents, "node_tokens": wl.node_tokens}
+        meta = {"D": wl.D, "bytes_per_seq": wl.logit_bytes() // wl.B}
+    else:
+        arrs = {"target": wl.target, "draft": wl.draft, "draft_tokens": wl.draft_tokens,
+                "uniforms": wl.uniforms}
+        meta = {"T": wl.T, "top_p": wl.top_p, "bytes_per_seq": wl.logit_bytes() // wl.B}
+    meta.update(B=wl.B, arrays=sorted(arrs))
     done, bytes_done, t0 = 0, 0, time.perf_counter()
     while True:
-        b = done % wl.B
-        sl = slice(b, b + 1)
-        if mode == "tree":
-            oracle.verify_tree(wl.target[sl], wl.parents, wl.node_tokens[sl], wl.D)
-            bytes_done += wl.N * wl.V * (4 if wl.dtype == workloads.F32 else 2)
-        else:
-            oracle.verify_sample(wl.target[sl], wl.draft[sl], wl.draft_tokens[sl],
-                                 wl.uniforms[sl], T=wl.T, top_p=wl.top_p)
-            bytes_done += wl.logit_bytes() // wl.B
+        bytes_done += _oracle_sequence(arrs, mode, done % wl.B, meta)
         done += 1
         el = time.perf_counter() - t0
         if el >= seconds:
             break
-    return {"value": bytes_done / el / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": "%d whole sequences of %s (round-robin over the batch), %.1f s on one core"
-                      % (done, wl.name, el),
-            "host_cores": os.cpu_count()}
+    one = {"value": bytes_done / el / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+           "sample": "%d whole sequences of %s (round-robin over the batch), %.1f s on one core"
+                     % (done, wl.name, el)}
+    cores = _host_cores()
+    if not all_cores or cores < 2:
+        return dict(one, host_cores=cores)
+    import multiprocessing as mp
+    per = max(1, int(round(done / el * seconds)))  # sequences per worker, about `seconds`
+    with tempfile.TemporaryDirectory() as folder:
+        for k, v in arrs.items():
+            np.save(os.path.join(folder, k + ".npy"), np.ascontiguousarray(v))
+        ctx = mp.get_context("spawn")
+        with ctx.Pool(cores) as pool:
+            pool.map(_oracle_worker, [(folder, mode, meta, w, 1) for w in range(cores)])  # start-up
+            t0 = time.perf_counter()
+            got = pool.map(_oracle_worker, [(folder, mode, meta, w * per, per)
+                                            for w in range(cores)])
+            el2 = time.perf_counter() - t0
+    # the baseline: every core; the one-core sample beside it
+    return {"value": sum(got) / el2 / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": "%d whole sequences of %s, %d per process on %d processes (one per core), "
+                      "%.1f s" % (per * cores, wl.name, per, cores, el2),
+            "host_cores": cores, "one_core": one}
+
+
+def chain_block(name, dev, peak, cpu_seconds, calls=100):
+    """Another chain workload, measured after the headline: best/median/mean
+    of `calls` whole calls and of the row-phase kernel alone, the roofline of
+    that kernel, and the one-core oracle on a bounded sample."""
+    import torch
+    wl, mode = make_workload(name)
+    job = Job(wl, mode, dev)
+    for i in range(3):
+        job.step(i)
+    torch.cuda.synchronize()
+    calls_t = per_call(call_times_ms(job.step, calls, job.stream))
+    rows_t = per_call(call_times_ms(job.rows_only, calls, job.stream))
+    job.step(0)
+    torch.cuda.synchronize()
+    nbytes = wl.logit_bytes(mode)
+    kern = "topp_kernel" if wl.top_p < 1.0 else "stream_kernel"
+    rows_gbs = nbytes / (rows_t["mean_us"] * 1e-6) / 1e9
+    call_gbs = nbytes / (calls_t["median_us"] * 1e-6) / 1e9
+    out = {"workload": describe(wl, mode)["workload"], "logit_bytes": nbytes,
+           "inputs_vs_l2": "two input copies of %.1f MB alternate between calls (L2: 126 MB)"
+                           % (nbytes / 1e6),
+           "ms_per_call": round(calls_t["median_us"] * 1e-3, 5), "calls": calls_t,
+           "gbs": round(call_gbs, 1), "frac": round(call_gbs / peak, 4),
+           "verify_calls_per_s": round(1e6 / calls_t["median_us"], 1),
+           "roofline": {"bound": "hbm", "kernel": kern, "avg_launch_us": rows_t["mean_us"],
+                        "launch": rows_t, "achieved": round(rows_gbs, 1), "peak": peak,
+                        "unit": "GB/s", "frac": round(rows_gbs / peak, 4),
+                        "traffic": profiled_traffic(kern, name), "algorithmic_bytes": nbytes},
+           "cpu_baseline": cpu_baseline(wl, mode, cpu_seconds, all_cores=False)}
+    del job
+    torch.cuda.empty_cache()
+    return out
+
+
+def tree_block(dev, peak, cpu_seconds, calls=100):
+    """c5 (greedy tree), with the stochastic tree (on c5's shape) and the
+    tree mask beside it."""
+    import torch
+    wl, mode = make_workload("c5")
+    job = Job(wl, mode, dev)
+    for i in range(3):
+        job.step(i)
+    torch.cuda.synchronize()
+    calls_t = per_call(call_times_ms(job.step, calls, job.stream))
+    nbytes = wl.logit_bytes(mode)
+    gbs = nbytes / (calls_t["median_us"] * 1e-6) / 1e9
+    out = {"workload": describe(wl, mode)["workload"], "logit_bytes": nbytes,
+           "ms_per_call": round(calls_t["median_us"] * 1e-3, 5), "calls": calls_t,
+           "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+           "roofline": {"bound": "hbm", "kernel": "stream_kernel+tree_kernel",
+                        "avg_launch_us": calls_t["mean_us"], "achieved": round(gbs, 1),
+                        "peak": peak, "unit": "GB/s", "frac": round(gbs / peak, 4),
+                        "traffic": None, "algorithmic_bytes": nbytes},
+           "cpu_baseline": cpu_baseline(wl, mode, cpu_seconds, all_cores=False)}
+    ts = timed_tree_sample(job)
+    ts["frac"] = round(ts["achieved_gbs"] / peak, 4)
+    out["tree_sample"] = ts
+    out["tree_mask"] = timed_tree_mask(job)
+    del job
+    torch.cuda.empty_cache()
+    return out
+
+
+def c1_block(dev, calls=200):
+    """c1 (B=1, k=3, V=32, fp32): the latency of one call; and its batched
+    form (10^5 replicated steps in one call): sequence steps per second."""
+    import torch
+    out = {}
+    for label, steps in (("B1_latency", 1), ("B100000", 100_000)):
+        wl = workloads.c1(steps=steps)
+        job = Job(wl, "stochastic", dev)
+        for i in range(3):
+            job.step(i)
+        torch.cuda.synchronize()
+        t = per_call(call_times_ms(job.step, calls if steps == 1 else 50, job.stream))
+        out[label] = {"B": wl.B, "k": wl.k, "V": wl.V, "calls": t,
+                      "sequence_steps_per_s": round(wl.B * 1e6 / t["median_us"], 1)}
+        del job
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_ours(args):
@@ -577,8 +787,19 @@ def run_ours(args):
     smi_index = visible.split(",")[local] if visible else str(local)
     clocks = ClockSampler(smi_index)
     time.sleep(0.3)
+    # The sampler polls every 20 ms: untimed calls before and after the
+    # timed ones keep the GPU under the same load for ~1 s around them.
+    nxt = soak(job, 0.0 if args.quick else 0.6)
     total_ms, rows_ms = timed_device(job, args.steps, args.warmup, world)
+    soak(job, 0.0 if args.quick else 0.4, nxt)
     clk = clocks.stop()
+    if clk is not None:
+        clk["window"] = ("the timed calls plus ~1 s of the same calls around them "
+                         "(20 ms sampling)")
+    # best / median / mean of individually timed calls (inputs alternate
+    # between two copies larger than L2)
+    calls = per_call(call_times_ms(job.step, 50 if args.quick else max(args.steps, 200),
+                                   job.stream))
     accept = timed_acceptance(job) if mode != "tree" else None
     probs = timed_probs(job) if mode != "tree" else None
     topk = timed_topk(job) if mode != "tree" else None
@@ -591,6 +812,7 @@ def run_ours(args):
     value = world * nbytes * args.steps / (total_ms * 1e-3) / 1e9
     peak, peak_kind = hbm_peak()
     e2e_ms, e2e_wall_ms, h2d, d2h = timed_e2e(job, args.e2e_steps)
+    h2d_peak = pinned_h2d_gbs(dev)
     e2e_ms = max_over_ranks(e2e_ms, world)
     e2e_value = world * nbytes * args.e2e_steps / (e2e_ms * 1e-3) / 1e9
 
@@ -619,8 +841,10 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
         "impl": "ours",
-        "config": dict(describe(wl, mode), l2="inputs %d MB > 126 MB L2, two input copies "
-                       "alternate between steps" % (nbytes // 10**6)),
+        "config": describe(wl, mode),
+        "inputs_vs_l2": ("inputs %d MB > 126 MB L2; two input copies alternate between steps"
+                         % (nbytes // 10**6)),
+        "calls": calls,
         "frac_of_peak": round(value / world / peak, 4), "peak_gbs": peak, "peak_kind": peak_kind,
         "frac_of_nominal_8tbs": round(value / world / 8000.0, 4),
         "verify_calls_per_s": round(world * args.steps / (total_ms * 1e-3), 1),
@@ -629,7 +853,10 @@ def run_ours(args):
         "roofline": roofline,
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "steps": args.e2e_steps,
                 "ms_per_step": round(e2e_ms / args.e2e_steps, 4),
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "h2d_pinned_gbs": h2d_peak,
+                "h2d_pinned_note": "one 256 MiB pinned host-to-device copy, repeated, timed "
+                                   "with CUDA events: the link rate the e2e copies share"},
         "gpu_launches": job.launches_per_step * args.steps,
         "clocks": clk,
     }
@@ -649,6 +876,14 @@ def run_ours(args):
         out["draft_probs"] = probs
     if rank == 0 and world == 1:
         out["cpu_baseline"] = cpu_baseline(wl, mode, args.cpu_seconds)
+    if rank == 0 and world == 1 and args.config == "c3" and not (args.no_blocks or args.quick):
+        # the other workloads, one block each (their own calls, after the
+        # headline's timed region)
+        cs = min(3.0, args.cpu_seconds)
+        out["configs"] = {"c4": chain_block("c4", dev, peak, cs),
+                          "c2": chain_block("c2", dev, peak, cs),
+                          "c5": tree_block(dev, peak, cs),
+                          "c1": c1_block(dev)}
     if rank == 0:
         print(json.dumps(out), flush=True)
 

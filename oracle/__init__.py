@@ -266,33 +266,47 @@ def verify_tree(target, parents, node_tokens, depth):
     return dict(tokens=out_t, num_accepted=out_n, path=out_p, errors=err)
 
 
-def boundary_flags(res, uniforms, top_p=1.0, tol=1e-5):
-    """Sequences whose outcome sits within `tol` of a decision boundary.
+def boundary_kinds(res, uniforms, top_p=1.0, tol=1e-5):
+    """Sequences whose outcome sits within `tol` of a decision boundary, by
+    kind, as three boolean arrays [B]:
 
-    A float32 implementation may legitimately decide such a sequence
-    differently from this fp64 oracle.  Flagged when, at any accept test the
-    oracle ran, |u_i - P_i / Q_i| < tol; or when |u - C(x-1)/S| or
-    |u - C(x)/S| < tol at the drawn token x; or (top-p) when a row's
-    cumulative mass before or at the threshold is within tol of top_p.
-    `res` must come from verify_sample(..., debug=True).
+    accept  -- at an accept test the oracle ran, |u_i - P_i / Q_i| < tol
+               (the accept count itself may differ in float32);
+    cdf     -- at the final draw, |u - C(x-1)/S| or |u - C(x)/S| < tol at
+               the drawn token x (only the drawn token may differ);
+    nucleus -- (top-p) a row's cumulative mass before or at its threshold
+               is within tol of top_p (its kept set, and with it any later
+               quantity, may differ).
+
+    Sequences the oracle rejected as invalid (num_accepted < 0) are never
+    flagged.  `res` must come from verify_sample(..., debug=True).
     """
     dbg, info = res["dbg"], res["row_info"]
     B = dbg.shape[0]
     k = (dbg.shape[1] - 3) // 2
     u = np.asarray(uniforms, np.float64).reshape(B, k + 1)
     j = res["num_accepted"]
+    valid = j >= 0
     P, Q = dbg[:, :k], dbg[:, k:2 * k]
     with np.errstate(divide="ignore", invalid="ignore"):
         ratio = np.where(Q > 0, P / Q, np.inf)
     tested = np.arange(k)[None, :] <= np.minimum(j, k - 1)[:, None]
-    flag = np.any(tested & (np.abs(u[:, :k] - ratio) < tol), axis=1)
+    acc = np.any(tested & (np.abs(u[:, :k] - ratio) < tol), axis=1)
     S, c0, c1 = dbg[:, 2 * k], dbg[:, 2 * k + 1], dbg[:, 2 * k + 2]
     with np.errstate(divide="ignore", invalid="ignore"):
-        flag |= (np.abs(u[:, k] - c0 / S) < tol) | (np.abs(u[:, k] - c1 / S) < tol)
+        cdf = (np.abs(u[:, k] - c0 / S) < tol) | (np.abs(u[:, k] - c1 / S) < tol)
+    nuc = np.zeros(B, bool)
     if top_p < 1.0:
         near = (np.abs(info[:, :, 2] - top_p) < tol) | (np.abs(info[:, :, 3] - top_p) < tol)
-        flag |= np.any(near, axis=1)
-    return flag & (j >= 0)
+        nuc = np.any(near, axis=1)
+    return acc & valid, cdf & valid, nuc & valid
+
+
+def boundary_flags(res, uniforms, top_p=1.0, tol=1e-5):
+    """Sequences within `tol` of any decision boundary (the union of
+    boundary_kinds)."""
+    acc, cdf, nuc = boundary_kinds(res, uniforms, top_p, tol)
+    return acc | cdf | nuc
 
 
 def verify_tree_sample(target, draft, parents, node_tokens, uniforms, depth, T=1.0, top_p=1.0,

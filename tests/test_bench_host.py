@@ -57,3 +57,32 @@ def test_profiled_traffic_needs_matching_code_and_workload(tmp_path, monkeypatch
     with open(src, "a") as f:
         f.write("__device__ int changed;\n")
     assert bench.profiled_traffic("k", "c3") is None
+
+
+def test_profile_sources_cover_every_included_file():
+    """Each profiled kernel's hash covers its translation unit and every file
+    it reaches through #include "...": a change to any of them (a shared
+    header, the C-ABI header) makes the committed capture stale."""
+    import re
+    for kernel, (_, sources) in bench.PROFILES.items():
+        names = {os.path.basename(p) for p in sources}
+        assert len(names) == len(sources)
+        for path in sources:
+            for inc in re.findall(r'^\s*#\s*include\s+"([^"]+)"', open(path).read(), flags=re.M):
+                assert os.path.basename(inc) in names, (kernel, path, inc)
+    assert {"topp.cu", "common.cuh", "stream.cuh", "spec_verify.h"} <= {
+        os.path.basename(p) for p in bench.PROFILES["topp_kernel"][1]}
+    assert {"rows.cu", "common.cuh", "stream.cuh", "spec_verify.h"} <= {
+        os.path.basename(p) for p in bench.PROFILES["stream_kernel"][1]}
+
+
+def test_include_closure_follows_nested_includes(tmp_path):
+    (tmp_path / "a.cu").write_text('#include "b.cuh"\n__global__ void k() {}\n')
+    (tmp_path / "b.cuh").write_text('#pragma once\n#include "c.h"\n')
+    (tmp_path / "c.h").write_text("#pragma once\n#include <stdint.h>\n")
+    got = [os.path.basename(p) for p in bench.include_closure(str(tmp_path / "a.cu"))]
+    assert got == ["a.cu", "b.cuh", "c.h"]
+    (tmp_path / "c.h").write_text('#include "missing.h"\n')
+    import pytest
+    with pytest.raises(FileNotFoundError):
+        bench.include_closure(str(tmp_path / "a.cu"))

@@ -84,9 +84,9 @@ def check(wl, beta, tv):
     assert np.all(err_b <= np.where(skip, np.inf, lim))
     assert np.all(err_t <= np.where(skip, np.inf, lim))
     # How many rows sit near the boundary is a property of the inputs (at
-    # small V each token moves the cumulative mass by ~1e-4): most pairs
-    # must still be compared.
-    assert skip[~nan].sum() <= max(2, 0.5 * (~nan).sum())
+    # small V each token moves the cumulative mass by ~1e-4); nearly every
+    # pair must still be compared.
+    assert skip[~nan].sum() <= max(2, 0.05 * (~nan).sum())
     return rb
 
 

@@ -15,6 +15,7 @@ pytestmark = [
 import oracle  # noqa: E402
 import speculative_decoding_verification_top_gb300 as sv  # noqa: E402
 import workloads  # noqa: E402
+import parity_rules  # noqa: E402
 from test_gpu_parity import DEV, _small_chain, dev  # noqa: E402
 
 
@@ -43,14 +44,8 @@ def run(wl, K, mode=sv.SPEC_STOCHASTIC):
 def check(wl, K, t, n, max_mismatch_frac=0.01):
     ref = oracle.verify_sample(wl.target, wl.draft, wl.draft_tokens, wl.uniforms, T=wl.T,
                                top_p=wl.top_p, top_k=K, debug=True)
-    flags = oracle.boundary_flags(ref, wl.uniforms, wl.top_p)
-    same = (n == ref["num_accepted"]) & np.all(t == ref["tokens"], axis=1)
-    bad = ~same & ~flags
-    print("%s K=%d top_p=%.2f: B=%d flagged=%d mismatched=%d accepted=%s" % (
-        wl.name, K, wl.top_p, wl.B, flags.sum(), (~same).sum(),
-        np.bincount(np.maximum(ref["num_accepted"], 0), minlength=wl.k + 1)))
-    assert not bad.any(), "unflagged mismatches at %s" % np.nonzero(bad)[0][:10]
-    assert (~same).sum() <= max(2, max_mismatch_frac * wl.B)
+    parity_rules.check("%s K=%d top_p=%.2f" % (wl.name, K, wl.top_p), t, n, ref, wl.uniforms,
+                       wl.top_p, max(2, int(max_mismatch_frac * wl.B)))
     return ref
 
 
@@ -79,7 +74,7 @@ def test_ragged_vocab(V, dtype, K, top_p):
     wl = _small_chain(6, 3, V, dtype, 0.8, top_p, seed=V + K)
     topk_tokens(wl, K, V)
     t, n, _ = run(wl, K)
-    check(wl, K, t, n, max_mismatch_frac=0.5)
+    check(wl, K, t, n, max_mismatch_frac=0.02)
 
 
 def test_ties_at_the_kth():
@@ -88,7 +83,7 @@ def test_ties_at_the_kth():
     wl = _small_chain(16, 3, 3000, workloads.BF16, 1.0, 1.0, seed=5, ties=True)
     topk_tokens(wl, 10, 5)
     t, n, _ = run(wl, 10)
-    check(wl, 10, t, n, max_mismatch_frac=0.5)
+    check(wl, 10, t, n, max_mismatch_frac=0.02)
 
 
 def test_k1_equals_greedy():
@@ -108,7 +103,7 @@ def test_k_beyond_the_near_max_list(K):
     wl = workloads.c4(B=6)
     topk_tokens(wl, K, 9)
     t, n, _ = run(wl, K)
-    check(wl, K, t, n, max_mismatch_frac=0.5)
+    check(wl, K, t, n, max_mismatch_frac=0.02)
 
 
 @pytest.mark.parametrize("K", [128, 129])
@@ -119,7 +114,7 @@ def test_at_the_warp_select_limit(K):
     wl = workloads.c4(B=6)
     topk_tokens(wl, K, 11)
     t, n, ws = run(wl, K)
-    check(wl, K, t, n, max_mismatch_frac=0.5)
+    check(wl, K, t, n, max_mismatch_frac=0.02)
     assert sv.last_error(ws) == 0
 
 
@@ -132,7 +127,7 @@ def test_rows_of_many_pieces(V):
     wl = _small_chain(2, 1, V, workloads.BF16, 0.8, 0.9, seed=V)
     topk_tokens(wl, 50, 7)
     t, n, ws = run(wl, 50)
-    check(wl, 50, t, n, max_mismatch_frac=0.5)
+    check(wl, 50, t, n, max_mismatch_frac=0.02)
     assert sv.last_error(ws) == 0
 
 
@@ -146,7 +141,7 @@ def test_flat_rows_overflow_the_list():
     for K in (10, 6000):
         topk_tokens(wl, K, K)
         t, n, _ = run(wl, K)
-        check(wl, K, t, n, max_mismatch_frac=0.5)
+        check(wl, K, t, n, max_mismatch_frac=0.02)
 
 
 def test_acceptance_and_probability_form():
@@ -173,6 +168,5 @@ def test_acceptance_and_probability_form():
     torch.cuda.synchronize()
     pref = oracle.verify_sample_probs(wl.target, q, toks, wl.uniforms, T=wl.T, top_p=wl.top_p,
                                       top_k=K, debug=True)
-    flags = oracle.boundary_flags(pref, wl.uniforms, wl.top_p)
-    same = (n.cpu().numpy() == pref["num_accepted"]) & np.all(t.cpu().numpy() == pref["tokens"], 1)
-    assert np.all(same | flags)
+    parity_rules.check("%s probs K=%d" % (wl.name, K), t.cpu().numpy(), n.cpu().numpy(), pref,
+                       wl.uniforms, wl.top_p, max(2, int(0.02 * wl.B)))

@@ -229,6 +229,15 @@ def c3(seed=3, B=64, V=151936):
 
 
 def c4(seed=4, B=128, V=128256):
+    """The top-p batch.  Its draft tokens come from a top-16 drafter over the
+    draft logits at temperature T (Gumbel-max restricted to the 16 largest),
+    not from the processed q (temperature and top-p 0.95): this module holds
+    none of the method's arithmetic, and top-p is part of it.  So the draws
+    are not x~ ~ q: about 1 in 384 lands on a token outside the draft's
+    nucleus, where q = 0 (every such draft is then accepted only if p > 0
+    there, by the ratio rule's q = 0 case).  Parity is unaffected (the step
+    is a fixed function of its inputs), but c4's acceptance statistics do
+    not describe the method's own x~ ~ q setting."""
     return zipf_chain("c4", B, 3, V, BF16, 0.7, 0.95, 1.5, 0.8, seed, drafter_top=16)
 
 
