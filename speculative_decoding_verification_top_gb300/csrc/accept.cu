@@ -282,7 +282,7 @@ int launch_accept_t(const AcceptArgs &base, bool masked, cudaStream_t st) {
     const int V = a.rows.V;
     if (!masked) {
         auto kernel = accept_kernel<T>;
-        const int ctas = resident_ctas(kernel, sizeof(T) == 2 ? 1 : 0);
+        const int ctas = resident_ctas(kernel, sizeof(T) == 2 ? 13 : 12);
         if (ctas <= 0) return SPEC_ERR_CUDA;
         const long long warps = static_cast<long long>(ctas) * kWarps;
         a.total = a.pairs * V;
@@ -294,7 +294,7 @@ int launch_accept_t(const AcceptArgs &base, bool masked, cudaStream_t st) {
         return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
     }
     auto qkernel = accept_queue_kernel<T>;
-    const int ctas = resident_ctas(qkernel, sizeof(T) == 2 ? 3 : 2);
+    const int ctas = resident_ctas(qkernel, sizeof(T) == 2 ? 15 : 14);
     if (ctas <= 0) return SPEC_ERR_CUDA;
     accept_list_kernel<T><<<static_cast<unsigned>((a.pairs + kWarps - 1) / kWarps), kThreads, 0, st>>>(a);
     if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;

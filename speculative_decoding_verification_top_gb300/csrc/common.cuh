@@ -796,10 +796,11 @@ struct TreeArgs {
 };
 
 // Resident CTAs of `kernel` (kThreads threads) on the current device,
-// cached per device and `slot`; 0 on a CUDA error.
+// cached per device and `slot`; 0 on a CUDA error.  Each kernel has a slot
+// of its own: rows.cu 0-3 and 8-9, final.cu 4-7, accept.cu 12-15.
 template <typename K>
 int resident_ctas(K kernel, int slot, size_t dsmem = 0) {
-    constexpr int kMaxDev = 64, kSlots = 12;
+    constexpr int kMaxDev = 64, kSlots = 16;
     static int cache[kMaxDev][kSlots];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev || slot < 0 ||
