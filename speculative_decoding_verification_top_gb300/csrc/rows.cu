@@ -124,6 +124,12 @@ int launch_stream_t(const RowView &rows, const SeqArgs &seq, int rows_total, flo
     long long seg = (a.total + warps - 1) / warps;
     seg = (seg + 7) / 8 * 8;
     a.seg = seg < kMinSeg ? kMinSeg : seg;
+    // Short rows (V <= kMinSeg) in a call that fits the grid: one row per
+    // segment, so that the rows' dependent steps (statistics, record,
+    // arrival, the decision) run on parallel warps rather than one after
+    // another on a single warp -- the latency of a small call.  (A row is
+    // then one piece.)
+    if (rows.V <= kMinSeg && static_cast<long long>(rows_total) <= warps) a.seg = rows.V;
     a.c = c;
     a.ws = ws;
     const long long used = (a.total + a.seg - 1) / a.seg;
