@@ -87,6 +87,7 @@ struct ChainPlan {
     int stoch, dtype, rows_total, use_topp, top_k;
     float c, temperature, top_p;
     cudaStream_t st;
+    int inline_draw;  // the rows kernel also draws (short rows, a whole call)
 };
 
 // qprob: draft_logits holds fp32 probabilities q [B, k, V], used as given
@@ -160,15 +161,21 @@ int plan_chain(const void *target_logits, const void *draft_logits, const int32_
     sq.uniforms = uniforms;
     sq.out_tokens = out_tokens;
     sq.out_num = out_num_accepted;
+    plan->inline_draw = 0;
     return SPEC_OK;
 }
 
 // Row statistics and accept decisions.  With top-p one kernel does both
 // for every row (statistics, then the nucleus), and takes the decisions.
-int launch_chain_rows(const ChainPlan &p) {
+// A whole stochastic call (logits form, no top-p or top-k) may also draw
+// there: on short rows laid out one row per warp, the deciding warp takes
+// its sequence's final draw and p.inline_draw is set.
+int launch_chain_rows(ChainPlan &p, bool whole) {
+    const bool offer = whole && p.stoch && !p.use_topp && !p.fin.qprob;
+    p.inline_draw = 0;
     if (!p.use_topp)
         return launch_stream_rows(p.rows, p.seq, p.rows_total, p.c, p.ws, p.stoch ? 0 : 1,
-                                  p.dtype, p.st);
+                                  p.dtype, p.st, offer ? &p.fin : nullptr, &p.inline_draw);
     ToppArgs ta;
     ta.rows = p.rows;
     ta.seq = p.seq;
@@ -182,7 +189,7 @@ int launch_chain_rows(const ChainPlan &p) {
 
 // Greedy verification completes inside the row kernel: nothing to finish.
 int launch_chain_finish(const ChainPlan &p) {
-    return p.stoch ? launch_final(p.fin, p.dtype, p.st) : SPEC_OK;
+    return p.stoch && !p.inline_draw ? launch_final(p.fin, p.dtype, p.st) : SPEC_OK;
 }
 
 }  // namespace
@@ -228,7 +235,7 @@ SPEC_EXPORT int spec_verify_sample(const void *target_logits, const void *draft_
                         top_p, mode, dtype, out_tokens, out_num_accepted, workspace,
                         workspace_bytes, stream, &plan);
     if (rc != SPEC_OK || B == 0) return rc;
-    rc = launch_chain_rows(plan);
+    rc = launch_chain_rows(plan, true);
     if (rc != SPEC_OK) return rc;
     return launch_chain_finish(plan);
 }
@@ -244,7 +251,7 @@ SPEC_EXPORT int spec_verify_sample_topk(const void *target_logits, const void *d
                         top_p, mode, dtype, out_tokens, out_num_accepted, workspace,
                         workspace_bytes, stream, &plan, false, top_k);
     if (rc != SPEC_OK || B == 0) return rc;
-    rc = launch_chain_rows(plan);
+    rc = launch_chain_rows(plan, true);
     if (rc != SPEC_OK) return rc;
     return launch_chain_finish(plan);
 }
@@ -260,7 +267,7 @@ SPEC_EXPORT int spec_verify_sample_rows(const void *target_logits, const void *d
                               temperature, top_p, mode, dtype, out_tokens, out_num_accepted,
                               workspace, workspace_bytes, stream, &plan);
     if (rc != SPEC_OK || B == 0) return rc;
-    return launch_chain_rows(plan);
+    return launch_chain_rows(plan, false);  // its finish call draws
 }
 
 SPEC_EXPORT int spec_verify_sample_finish(const void *target_logits, const void *draft_logits,
@@ -288,7 +295,7 @@ SPEC_EXPORT int spec_verify_sample_probs(const void *target_logits, const float 
                         top_p, SPEC_STOCHASTIC, dtype, out_tokens, out_num_accepted, workspace,
                         workspace_bytes, stream, &plan, true, top_k);
     if (rc != SPEC_OK || B == 0) return rc;
-    rc = launch_chain_rows(plan);
+    rc = launch_chain_rows(plan, true);
     if (rc != SPEC_OK) return rc;
     return launch_chain_finish(plan);
 }

@@ -693,36 +693,30 @@ __device__ __forceinline__ void greedy_sequence(const RowView &v, const SeqArgs 
 
 // Called by a whole warp right after its lane 0 wrote row `row`'s record:
 // counts the row towards its sequence and, for the sequence's last row,
-// runs the sequence's completion step.
+// runs the sequence's completion step.  Returns the sequence whose accept
+// decision this warp took (kSeqDecide), else -1.
 template <typename T>
-__device__ __forceinline__ void row_done(const RowView &v, const SeqArgs &sa,
-                                         const Workspace &ws, float c, int row) {
-    if (sa.work == kSeqNone) return;
+__device__ __forceinline__ int row_done(const RowView &v, const SeqArgs &sa,
+                                        const Workspace &ws, float c, int row) {
+    if (sa.work == kSeqNone) return -1;
     const int lane = threadIdx.x & 31;
     const int b = row / v.R;
     int last = 0;
     if (lane == 0) last = arrive(&ws.seq_rows[b], 1u) == static_cast<unsigned>(v.R - 1);
     last = __shfl_sync(0xFFFFFFFFu, last, 0);
     __syncwarp();
-    if (!last) return;
+    if (!last) return -1;
     if (lane == 0) ws.seq_rows[b] = 0u;
     if (sa.work == kSeqDecide) {
         if (sa.qprob) decide_sequence<T, true>(v, sa, ws, c, b);
         else decide_sequence<T, false>(v, sa, ws, c, b);
+        return b;
     }
-    else greedy_sequence(v, sa, ws, b);
+    greedy_sequence(v, sa, ws, b);
+    return -1;
 }
 
 // ----------------------------------------------------------- launchers
-
-struct StreamArgs {
-    RowView rows;
-    SeqArgs seq;
-    long long total;   // elements over all rows
-    long long seg;     // elements per warp segment
-    float c;           // log2(e) / temperature
-    Workspace ws;
-};
 
 struct ToppArgs {
     RowView rows;
@@ -747,6 +741,16 @@ struct FinalArgs {
     int32_t *out_tokens;
     int32_t *out_num;
     Workspace ws;
+};
+
+struct StreamArgs {
+    RowView rows;
+    SeqArgs seq;
+    long long total;   // elements over all rows
+    long long seg;     // elements per warp segment
+    float c;           // log2(e) / temperature
+    Workspace ws;
+    FinalArgs fin;     // kind 3: the final draw's arguments
 };
 
 struct AcceptArgs {
@@ -821,7 +825,8 @@ int resident_ctas(K kernel, int slot, size_t dsmem = 0) {
 // kind 0: stochastic statistics; kind 1: argmax.  dtype: SPEC_F32 /
 // SPEC_BF16.  Each returns SPEC_OK or SPEC_ERR_CUDA.
 int launch_stream_rows(const RowView &rows, const SeqArgs &seq, int rows_total, float c,
-                       const Workspace &ws, int kind, int dtype, cudaStream_t st);
+                       const Workspace &ws, int kind, int dtype, cudaStream_t st,
+                       const FinalArgs *fin = nullptr, int *drew = nullptr);
 // Stochastic statistics plus every row's summary (top-p's first phase);
 // *seg gets the warp segment used (the summary's layout depends on it).
 int launch_stream_summary(const RowView &rows, int rows_total, float c, const Workspace &ws,

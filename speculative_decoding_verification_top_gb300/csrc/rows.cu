@@ -22,8 +22,16 @@
 //                 each lane's batch of vectors, stream.cuh) that the top-k
 //                 select reads (select.cu, topp.cu).  With top-p or top-k
 //                 the decisions wait for the nucleus: the select kernels
-//                 take them.
+//                 take them.  Kind 3 is kind 0 whose deciding warp also
+//                 takes the sequence's final draw (draw.cuh, the same steps
+//                 as final.cu's warps), so that no final kernel follows: a
+//                 whole call on short rows laid out one row per warp, where
+//                 a warp decides at most one sequence and the two launches'
+//                 latency chain is the call's time.  (It is a kernel of its
+//                 own because the draw's registers would cut kind 0's
+//                 residency.)
 
+#include "draw.cuh"
 #include "stream.cuh"
 
 namespace specv {
@@ -51,7 +59,7 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(const StreamArgs a) {
         float m = kNegInf, s = 0.0f;
         int arg = INT_MAX;
         uint32_t fl = 0;
-        if (KIND == 0) {
+        if (KIND == 0 || KIND == 3) {
             warp_piece_ms<T>(rowp, lo, hi, a.c, m, s, fl);
             warp_reduce_ms(m, s, fl, a.c);
         } else if (KIND == 2) {
@@ -69,7 +77,11 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(const StreamArgs a) {
         RowRec *dst = a.ws.rows + row;
         if (pieces == 1) {
             if (lane == 0) write_row(dst, m, s, arg, fl);
-            row_done<T>(a.rows, a.seq, a.ws, a.c, row);
+            const int bd = row_done<T>(a.rows, a.seq, a.ws, a.c, row);
+            if (KIND == 3 && bd >= 0) {
+                __syncwarp();  // the decision record, written by several lanes
+                draw_run<T, false>(a.fin, bd, 0, a.fin.NS);
+            }
         } else {
             int last = 0;
             if (lane == 0) {
@@ -100,7 +112,11 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(const StreamArgs a) {
                 if (KIND != 1) warp_reduce_ms(m, s, fl, a.c);
                 else warp_reduce_arg(m, arg, fl);
                 if (lane == 0) write_row(dst, m, s, arg, fl);
-                row_done<T>(a.rows, a.seq, a.ws, a.c, row);
+                const int bd = row_done<T>(a.rows, a.seq, a.ws, a.c, row);
+                if (KIND == 3 && bd >= 0) {
+                    __syncwarp();  // the decision record, written by several lanes
+                    draw_run<T, false>(a.fin, bd, 0, a.fin.NS);
+                }
             }
         }
         s0 += hi - lo;
@@ -109,9 +125,12 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(const StreamArgs a) {
 
 // ------------------------------------------------- grid sizing (host)
 
+// fin (kind 0 only): a whole call's final-draw arguments; when the layout
+// is one row per warp, kind 3 runs instead and *drew is set to 1.
 template <typename T, int KIND>
 int launch_stream_t(const RowView &rows, const SeqArgs &seq, int rows_total, float c,
-                    const Workspace &ws, cudaStream_t st, long long *seg_out = nullptr) {
+                    const Workspace &ws, cudaStream_t st, long long *seg_out = nullptr,
+                    const FinalArgs *fin = nullptr, int *drew = nullptr) {
     auto kernel = stream_kernel<T, KIND>;
     const int ctas = resident_ctas(kernel, KIND == 2 ? (sizeof(T) == 2 ? 9 : 8)
                                                      : (sizeof(T) == 2 ? 2 : 0) + KIND);
@@ -132,21 +151,31 @@ int launch_stream_t(const RowView &rows, const SeqArgs &seq, int rows_total, flo
     if (rows.V <= kMinSeg && static_cast<long long>(rows_total) <= warps) a.seg = rows.V;
     a.c = c;
     a.ws = ws;
+    a.fin = FinalArgs{};
     const long long used = (a.total + a.seg - 1) / a.seg;
     const unsigned grid = static_cast<unsigned>((used + kWarps - 1) / kWarps);
     if (seg_out) *seg_out = a.seg;
-    kernel<<<grid, kThreads, 0, st>>>(a);
+    if (KIND == 0 && fin && a.seg == rows.V) {
+        a.fin = *fin;
+        if (drew) *drew = 1;
+        stream_kernel<T, 3><<<grid, kThreads, 0, st>>>(a);
+    } else {
+        kernel<<<grid, kThreads, 0, st>>>(a);
+    }
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
 }  // namespace
 
 int launch_stream_rows(const RowView &rows, const SeqArgs &seq, int rows_total, float c,
-                       const Workspace &ws, int kind, int dtype, cudaStream_t st) {
+                       const Workspace &ws, int kind, int dtype, cudaStream_t st,
+                       const FinalArgs *fin, int *drew) {
     if (dtype == SPEC_F32)
-        return kind == 0 ? launch_stream_t<float, 0>(rows, seq, rows_total, c, ws, st)
+        return kind == 0 ? launch_stream_t<float, 0>(rows, seq, rows_total, c, ws, st, nullptr,
+                                                     fin, drew)
                          : launch_stream_t<float, 1>(rows, seq, rows_total, c, ws, st);
-    return kind == 0 ? launch_stream_t<uint16_t, 0>(rows, seq, rows_total, c, ws, st)
+    return kind == 0 ? launch_stream_t<uint16_t, 0>(rows, seq, rows_total, c, ws, st, nullptr,
+                                                    fin, drew)
                      : launch_stream_t<uint16_t, 1>(rows, seq, rows_total, c, ws, st);
 }
 

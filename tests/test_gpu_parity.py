@@ -74,16 +74,26 @@ def check_intermediates(wl, ws, ref, flags):
     rtol = 1e-5 if wl.dtype == workloads.F32 else 2e-3
     k = wl.k
     rP, rQ = ref["dbg"][:, :k], ref["dbg"][:, k:2 * k]
+    # P, Q and the recorded normaliser are taken over the nucleus: on a
+    # sequence with a row whose prefix mass lies at top_p (the oracle's
+    # nucleus flag) the kept set, and so that normaliser, depends on the
+    # order of the sums.
+    nuc = oracle.boundary_kinds(ref, wl.uniforms, wl.top_p)[2]
+    pq = ok & ~nuc
+    print("%s P/Q compared on %d of %d sequences (nucleus-flagged: %d)"
+          % (wl.name, pq.sum(), ok.sum(), (ok & nuc).sum()))
     for got, want, name in ((P, rP, "P"), (Q, rQ, "Q")):
-        err = np.abs(got - want)[ok]
-        lim = (rtol * np.abs(want) + 1e-30)[ok]
-        print("%s %s max rel err %.3g" % (wl.name, name, (err / np.maximum(np.abs(want[ok]), 1e-30)).max()))
+        if not pq.any():
+            continue
+        err = np.abs(got - want)[pq]
+        lim = (rtol * np.abs(want) + 1e-30)[pq]
+        print("%s %s max rel err %.3g" % (wl.name, name, (err / np.maximum(np.abs(want[pq]), 1e-30)).max()))
         assert np.all(err <= lim), name
     info = ref["row_info"]
     rZ = info[:, :, 0] * info[:, :, 3]
-    zerr = (np.abs(Z - rZ) / rZ)[ok]
-    print("%s Z max rel err %.3g" % (wl.name, zerr.max()))
-    assert zerr.max() <= rtol
+    zerr = (np.abs(Z - rZ) / rZ)[pq]
+    print("%s Z max rel err %.3g" % (wl.name, zerr.max() if zerr.size else 0.0))
+    assert np.all(zerr <= rtol)
     # S is compared where both sides drew from the same row.
     same_j = ok & ~flags
     serr = np.abs(S - ref["dbg"][:, 2 * k])[same_j]
@@ -167,7 +177,8 @@ def _small_chain(B, k, V, dtype, T, top_p, seed, ties=False):
                            workloads.uniforms(rng, (B, k + 1)))
 
 
-@pytest.mark.parametrize("V", [1, 7, 8, 9, 33, 1000, 8191, 8193, 16383, 16384, 16385, 40001])
+@pytest.mark.parametrize("V", [1, 7, 8, 9, 33, 1000, 1025, 2048, 2049, 8191, 8193, 16383,
+                               16384, 16385, 40001])
 @pytest.mark.parametrize("dtype", [workloads.F32, workloads.BF16])
 def test_ragged_vocab(V, dtype):
     for top_p in (1.0, 0.9):
@@ -275,8 +286,13 @@ def test_repeated_calls_are_bitwise_reproducible():
         np.testing.assert_array_equal(a, b)
 
 
-@pytest.mark.parametrize("make", [lambda: workloads.c4(B=4), lambda: workloads.c3(B=6)],
-                         ids=["top_p_rows", "stream_rows"])
+@pytest.mark.parametrize("make", [
+    lambda: workloads.c4(B=4), lambda: workloads.c3(B=6),
+    # short rows, one row per warp: the whole call draws inside the rows
+    # kernel, the two-phase call in the final kernel (NS = 1 and 2 sub-tiles)
+    lambda: _small_chain(40, 3, 1000, workloads.F32, 0.8, 1.0, seed=11),
+    lambda: _small_chain(40, 4, 2048, workloads.BF16, 1.2, 1.0, seed=12)],
+    ids=["top_p_rows", "stream_rows", "short_rows_f32", "short_rows_bf16"])
 def test_two_phase_api_equals_single_call(make):
     wl = make()
     t1, n1, _ = run_gpu(wl)
@@ -287,8 +303,9 @@ def test_two_phase_api_equals_single_call(make):
     ws = sv.new_workspace(nbytes, DEV)
     stream = torch.cuda.current_stream().cuda_stream
     args = (tg.data_ptr(), dr.data_ptr(), tk.data_ptr(), un.data_ptr(), wl.B, wl.k, wl.V, wl.T,
-            wl.top_p, sv.SPEC_STOCHASTIC, sv.SPEC_BF16, out_t.data_ptr(), out_n.data_ptr(),
-            ws.data_ptr(), ws.numel(), stream)
+            wl.top_p, sv.SPEC_STOCHASTIC,
+            sv.SPEC_BF16 if wl.dtype == workloads.BF16 else sv.SPEC_F32,
+            out_t.data_ptr(), out_n.data_ptr(), ws.data_ptr(), ws.numel(), stream)
     sv.spec_verify_sample_rows(*args)
     sv.spec_verify_sample_finish(*args)
     torch.cuda.synchronize()
