@@ -176,12 +176,16 @@ int spec_verify_sample_topk(const void *target_logits, const void *draft_logits,
 
 /*
  * The two phases of spec_verify_sample, with the same arguments.
- * spec_verify_sample == spec_verify_sample_rows followed, on the same
- * stream and workspace, by spec_verify_sample_finish.
- *   _rows    streams every logit row once and leaves per-row statistics
- *            (max, normaliser, nucleus threshold, argmax) in the workspace;
- *   _finish  reads them, runs the accept scan and the final draw, and
- *            writes out_tokens / out_num_accepted.
+ * spec_verify_sample gives the results of spec_verify_sample_rows followed,
+ * on the same stream and workspace, by spec_verify_sample_finish, bit for
+ * bit.  (On a small call with short rows it launches no separate draw: the
+ * row kernel's deciding warp draws.)
+ *   _rows    streams every logit row once, leaves per-row statistics
+ *            (max, normaliser, nucleus threshold, argmax) in the workspace
+ *            and takes every sequence's accept decision; with top-p it also
+ *            draws from the nucleus list and writes those outputs;
+ *   _finish  runs the remaining final draws (residual or bonus row) and
+ *            writes out_tokens / out_num_accepted for them.
  * The split lets a caller time or overlap the phases; _finish must follow a
  * _rows call with identical arguments, with no other call on the workspace
  * in between.  In SPEC_GREEDY mode _rows does all the work and _finish
