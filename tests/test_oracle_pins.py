@@ -239,6 +239,33 @@ def test_greedy_first_maximum():
     assert res["num_accepted"][0] == 1 and list(res["tokens"][0]) == [1, 0]
 
 
+def test_argmax_row_is_numpys_first_maximum():
+    """Reading R5 (the greedy rule's argmax is the first maximum of the raw
+    logits) reduces to numpy's argmax, which returns the first occurrence:
+    random rows with planted ties, fp32 and bf16, rows holding -inf; a NaN
+    or +inf fails the row, and so does a row of -inf only."""
+    rng = np.random.default_rng(21)
+    for V in (1, 2, 7, 33, 1000):
+        for _ in range(20):
+            row = np.round(rng.normal(0, 2, V) * 2).astype(np.float32) / 2  # ties
+            if V > 2:
+                row[rng.integers(0, V, 2)] = -np.inf
+                row[rng.integers(0, V)] = row.max()  # a second copy of the max
+            if np.isneginf(row).all():
+                continue
+            st, arg = oracle.argmax_row(row)
+            assert st == 0 and arg == int(np.argmax(row)), (V, row)
+            bits = workloads.to_bf16_bits(row)
+            st, arg = oracle.argmax_row(bits)
+            assert st == 0 and arg == int(np.argmax(workloads.as_f32(bits)))
+    ok = np.array([0.5, 2.0, -1.0], np.float32)
+    for bad in (np.nan, np.inf):
+        row = ok.copy()
+        row[2] = bad
+        assert oracle.argmax_row(row)[0] == 1
+    assert oracle.argmax_row(np.full(4, -np.inf, np.float32))[0] == 2
+
+
 def test_inverse_cdf_against_searchsorted():
     """The draw is the textbook inverse CDF: numpy's searchsorted of u*S in
     the cumulative sums, side='right'."""
