@@ -353,7 +353,11 @@ int spec_verify_tree_mask(const int32_t *parents, const int32_t *pos0, int B, in
  *     first.  All calls on a device share the one array: calls whose work
  *     overlaps on the GPU race and give wrong results; order them.
  *   - The first call on a device looks up the array's device address (with
- *     that device current); make it before any stream capture begins.
+ *     that device current); make it before any stream capture begins.  The
+ *     address is kept for the process and belongs to the device's primary
+ *     context (the one the CUDA runtime uses): do not call this entry point
+ *     from another context on that device, nor after resetting the device
+ *     (cudaDeviceReset) once it has been called there.
  *   - Data errors show as -1 outputs; the error word is not kept.
  */
 int spec_verify_sample_noalloc(const void *target_logits, const void *draft_logits,
